@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark: useful (unmasked) attention TFLOP/s of one forward + backward step on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input: the planner and
+forward kernel (out, lse), then the backward planner, preprocess, backward kernel and dq
+conversion (dq, dk, dv).  Useful FLOPs per step = (4 + 10) * d * Hq * V, V = visible
+(query, key) pairs under union semantics (forward: two GEMMs, backward: five, 2 flops per
+multiply-add); masked work inside partial tiles is not counted.
+
+Default workload: 65536 packed tokens, Hq 16 / Hkv 4, d 128, one CAUSAL slice over all
+tokens plus two FULL slices over a 4096-token prefix (bf16 N(0,1), seed 3).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+--impl reference times the float64 CPU oracle (a deliberately slow baseline) on a bounded
+sample of the same workload.  With N > 1 (torchrun), every rank runs an independent replica
+of the workload on its own GPU: the attention has no cross-GPU exchange.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "unmasked attention TFLOP/s fwd/bwd on 1 GB300; % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def visible_pairs(w: W.Workload) -> int:
+    """Exact visible-pair count from the slice list (per-row interval union, host-side)."""
+    # Rows are processed in blocks; each row's visible set is the union of one interval per
+    # slice that covers it.  Pure counting, no attention arithmetic.
+    total = w.total
+    qr = np.asarray(w.q_ranges, dtype=np.int64).reshape(-1, 2)
+    kr = np.asarray(w.k_ranges, dtype=np.int64).reshape(-1, 2)
+    ty = np.asarray(w.types, dtype=np.int64)
+    keep = (qr[:, 0] < qr[:, 1]) & (kr[:, 0] < kr[:, 1])
+    qr, kr, ty = qr[keep], kr[keep], ty[keep]
+    n = 0
+    for r0 in range(0, total, 8192):
+        rows = np.arange(r0, min(total, r0 + 8192))[:, None]
+        sel = (qr[:, 0] < rows[-1, 0] + 1) & (qr[:, 1] > r0)
+        if not sel.any():
+            continue
+        qs, qe, ks, ke, t = qr[sel, 0], qr[sel, 1], kr[sel, 0], kr[sel, 1], ty[sel]
+        inside = (rows >= qs) & (rows < qe)
+        hi = np.where(t == 1, np.minimum(ke, rows + ke - qe + 1), ke)
+        lo = np.broadcast_to(ks, hi.shape)
+        hi = np.where(inside, np.maximum(hi, lo), lo)
+        order = np.argsort(np.where(hi > lo, lo, 1 << 60), axis=1, kind="stable")
+        lo_s = np.take_along_axis(lo, order, 1)
+        hi_s = np.take_along_axis(hi, order, 1)
+        cur = np.full(rows.shape[0], -1, dtype=np.int64)
+        for c in range(lo_s.shape[1]):
+            a, b = lo_s[:, c], hi_s[:, c]
+            valid = b > a
+            st = np.maximum(a, cur)
+            n += int(np.where(valid, np.maximum(0, b - st), 0).sum())
+            cur = np.where(valid, np.maximum(cur, b), cur)
+    return n
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str):
+        self.gpu, self.path, self.proc = gpu_index, path, None
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                s = float(parts[1].split()[0]); mx = float(parts[2].split()[0])
+            except ValueError:
+                continue
+            smax = mx
+            sm.append(s)
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"]}
+        loaded = [x for x in sm if x >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def smi_index(cuda_index: int) -> int:
+    """nvidia-smi index of a CUDA device (honours CUDA_VISIBLE_DEVICES when it lists indices)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    if cuda_index < len(ids) and ids[cuda_index].isdigit():
+        return int(ids[cuda_index])
+    return cuda_index
+
+
+def dist_setup(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a host float over ranks (host-side timing reduction, not a data-path collective)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def make_inputs(w: W.Workload):
+    q, k, v, do = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed)
+    qr, kr, ty = W.ranges_tensors(w.padded())
+    return q, k, v, do, qr, kr, ty
+
+
+def run_ours(args, w: W.Workload, rank: int, world: int, local: int):
+    import flexible_mask_attention_range_gb300 as ffa
+    from flexible_mask_attention_range_gb300 import build as ffa_build
+    ffa_build.ensure_built()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    V = visible_pairs(w)
+    fl_fwd = 4.0 * w.d * w.hq * V
+    fl_bwd = 10.0 * w.d * w.hq * V
+    q_h, k_h, v_h, do_h, qr_h, kr_h, ty_h = make_inputs(w)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    qr, kr, ty = (t.to(dev) for t in (qr_h, kr_h, ty_h))
+    out = torch.empty_like(q)
+    lse = torch.empty(w.hq, w.total, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    R = qr.shape[0]
+    wsf = torch.empty(ffa.ffa_fwd_workspace_size(w.total, w.total, w.hq, w.hkv, w.d, R), dtype=torch.uint8,
+                      device=dev)
+    wsb = torch.empty(ffa.ffa_bwd_workspace_size(w.total, w.total, w.hq, w.hkv, w.d, R), dtype=torch.uint8,
+                      device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = w.softmax_scale
+
+    def step():
+        ffa.ffa_fwd(q, k, v, qr, kr, ty, scale, w.softcap, out=out, lse=lse, workspace=wsf, status=status)
+        ffa.ffa_bwd(q, k, v, out, lse, do, qr, kr, ty, scale, w.softcap, dq=dq, dk=dk, dv=dv, workspace=wsb,
+                    status=status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+
+    # ---- device-timed region: K steps, events around every main kernel launch
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clock_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
+    os.makedirs(os.path.dirname(clock_path), exist_ok=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(smi_index(dev.index), clock_path) as clk:
+        time.sleep(0.3)
+        t0.record()
+        for i in range(K):
+            ffa.ffa_set_kernel_events(*ev[i])
+            step()
+        t1.record()
+        ffa.ffa_set_kernel_events()
+        torch.cuda.synchronize()
+        time.sleep(0.2)
+    barrier(world)
+    ms_total = t0.elapsed_time(t1)
+    ms_step = max_over_ranks(ms_total / K, world)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    clocks = clk.summary()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+    value = world * (fl_fwd + fl_bwd) / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    q_p, k_p, v_p, do_p = (t.pin_memory() for t in (q_h, k_h, v_h, do_h))
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq_h, dk_h, dv_h = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+    h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p, do_p, qr_h, kr_h, ty_h))
+    d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h, dq_h, dk_h, dv_h))
+    E = max(2, min(K, 5))
+
+    def e2e_step():
+        q.copy_(q_p, non_blocking=True); k.copy_(k_p, non_blocking=True); v.copy_(v_p, non_blocking=True)
+        do.copy_(do_p, non_blocking=True)
+        qr.copy_(qr_h, non_blocking=True); kr.copy_(kr_h, non_blocking=True); ty.copy_(ty_h, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True); lse_h.copy_(lse, non_blocking=True)
+        dq_h.copy_(dq, non_blocking=True); dk_h.copy_(dk, non_blocking=True); dv_h.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(E):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, world)
+    e2e_value = world * (fl_fwd + fl_bwd) / (e2e_ms * 1e-3) / 1e12
+
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1900.0)))
+    bwd_tf = fl_bwd / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = fl_fwd / (fwd_ms * 1e-3) / 1e12
+    traffic = read_profile_traffic(w.name)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "total_seqlen": w.total, "num_heads_q": w.hq, "num_heads_kv": w.hkv,
+                   "head_dim": w.d, "slices": len(w.types), "softcap": w.softcap, "visible_pairs": V,
+                   "pass": "fwd+bwd", "l2": "inputs larger than L2 (q alone is "
+                   f"{w.total * w.hq * w.d * 2 / 2**20:.0f} MiB)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
+        "fwd_kernel_ms": round(fwd_ms, 4), "bwd_kernel_ms": round(bwd_ms, 4),
+        "frac_of_peak": {"fwd": round(fwd_tf / peak_t, 4), "bwd": round(bwd_tf / peak_t, 4),
+                         "step": round(value / world / peak_t, 4), "peak": f"bf16_tflops_sustained of {peak_src}"},
+        "roofline": {"kernel": "ffa_bwd_kernel", "bound": "tensor", "achieved": round(bwd_tf, 2),
+                     "peak": peak_t, "unit": "TFLOP/s", "frac": round(bwd_tf / peak_t, 4),
+                     "traffic": traffic.get("ffa_bwd_kernel"), "peak_source": f"{peak_src} sustained bf16"},
+        "roofline_fwd": {"kernel": "ffa_fwd_kernel", "bound": "tensor", "achieved": round(fwd_tf, 2),
+                         "peak": peak_t, "unit": "TFLOP/s", "frac": round(fwd_tf / peak_t, 4),
+                         "traffic": traffic.get("ffa_fwd_kernel")},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": K * GPU_LAUNCHES_PER_STEP,
+        "clocks": clocks,
+    }
+    return result, (q_h, k_h, v_h, do_h)
+
+
+# planner (slices, rows, order) + forward; planner (slices, cols, order) + pre + backward + convert
+GPU_LAUNCHES_PER_STEP = 4 + 6
+
+
+def read_profile_traffic(workload: str):
+    """Per-launch DRAM bytes of the main kernels from the committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return {}
+    try:
+        d = json.load(open(p))
+        return d.get(workload, {})
+    except Exception:
+        return {}
+
+
+def oracle_sample(w: W.Workload, inputs, rows: np.ndarray):
+    """Time the float64 oracle on a bounded sample: forward + dq for the given rows."""
+    import oracle as O
+    q, k, v, do = inputs
+    t0 = time.perf_counter()
+    O.forward(q, k, v, w.q_ranges, w.k_ranges, w.types, softmax_scale=w.softmax_scale, softcap=w.softcap,
+              rows=rows)
+    O.backward(q, k, v, do, w.q_ranges, w.k_ranges, w.types, softmax_scale=w.softmax_scale, softcap=w.softcap,
+               rows=rows)
+    dt = time.perf_counter() - t0
+    # useful flops of the sample: forward 4 d Hq per visible pair, dq-only backward 6 d Hq
+    qr = np.asarray(w.q_ranges, dtype=np.int64).reshape(-1, 2)
+    kr = np.asarray(w.k_ranges, dtype=np.int64).reshape(-1, 2)
+    ty = np.asarray(w.types)
+    pairs = 0
+    for i in rows:
+        ivs = []
+        for (qs, qe), (ks, ke), t in zip(qr, kr, ty):
+            if qs <= i < qe and ks < ke:
+                hi = min(ke, i + ke - qe + 1) if t == 1 else ke
+                if hi > ks:
+                    ivs.append((ks, hi))
+        ivs.sort()
+        cur = -1
+        for a, b in ivs:
+            a = max(a, cur)
+            if b > a:
+                pairs += b - a
+            cur = max(cur, b)
+    flops = (4.0 + 6.0) * w.d * w.hq * pairs
+    return dt, flops
+
+
+def cpu_threads() -> int:
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def sample_rows(w: W.Workload, n: int, seed: int):
+    g = np.random.default_rng(seed)
+    return np.sort(g.choice(w.total, size=n, replace=False))
+
+
+def run_reference(args, w: W.Workload):
+    inputs = make_inputs(w)[:4]
+    rows_per_step = 6
+    for i in range(args.warmup):
+        oracle_sample(w, inputs, sample_rows(w, rows_per_step, 1000 + i))
+    times, flops = [], []
+    for i in range(args.steps):
+        dt, fl = oracle_sample(w, inputs, sample_rows(w, rows_per_step, i))
+        times.append(dt)
+        flops.append(fl)
+    value = sum(flops) / sum(times) / 1e12
+    cores = cpu_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "total_seqlen": w.total, "num_heads_q": w.hq, "num_heads_kv": w.hkv,
+                   "head_dim": w.d, "pass": "fwd+bwd(dq) on sampled rows"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} random query rows per step (forward + dq over each "
+                                   "row's full key set, all heads), float64 numpy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_causal_64k_prefix", choices=W.ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = W.get(args.workload)
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    result, inputs = run_ours(args, w, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            rows = sample_rows(w, 8, 77)
+            dt, fl = oracle_sample(w, inputs, rows)
+            result["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": UNIT, "cores": cpu_threads(),
+                                      "kind": "oracle", "seconds": round(dt, 2),
+                                      "sample": "8 random query rows (forward + dq over each row's full key "
+                                                "set, all heads), float64 numpy"}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,262 @@
+"""GB300 (sm_103a) range-masked flash attention: thin Python binding over libffa.so.
+
+Every function here only marshals arguments: it checks tensor properties, allocates outputs
+and the workspace with torch, and passes raw device pointers and the current CUDA stream to
+the C ABI declared in include/ffa.h.  All computation runs in the library's CUDA kernels;
+there is no fallback.  If libffa.so has not been built, importing works but every call
+raises.
+
+Interface after flex_flash_attn_func (MagiAttention issue #180): packed q [Nq, Hq, d],
+k/v [Nk, Hkv, d] in bf16, slices q_ranges/k_ranges int32 [R, 2] and attn_type_map int32 [R]
+(0 = FULL, 1 = CAUSAL); slices with start == end are no-ops.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+FULL = 0
+CAUSAL = 1
+TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
+STATUS_BAD_RANGE = 1
+STATUS_TIMEOUT = 2
+TILE = 128
+
+
+class FfaShape(ctypes.Structure):
+    _fields_ = [("total_q", ctypes.c_int64), ("total_k", ctypes.c_int64),
+                ("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32)]
+
+
+class FfaError(RuntimeError):
+    pass
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+# exported symbol -> (restype, argtypes), mirroring include/ffa.h
+SIGNATURES = {
+    "ffa_fwd_workspace_size": (_SZ, [ctypes.POINTER(FfaShape), _I32]),
+    "ffa_bwd_workspace_size": (_SZ, [ctypes.POINTER(FfaShape), _I32]),
+    "ffa_fwd": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _I32, _F, _F, _P, _P, _P,
+                               _SZ, _P, _P]),
+    "ffa_bwd": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _F, _F,
+                               _P, _P, _P, _P, _SZ, _P, _P]),
+    "ffa_plan_tiles": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _I32, _I32, _P, _P, _SZ, _P,
+                                      _P]),
+    "ffa_set_kernel_events": (ctypes.c_int, [_P, _P, _P, _P]),
+    "ffa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "ffa_build_info": (ctypes.c_char_p, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libffa.so.  Raises if it has not been built (no fallback exists)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise FfaError(f"{path} is not built; run flexible_mask_attention_range_gb300.build.build() "
+                           "(nvcc, sm_103a) first")
+        h = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(h, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = h
+    return _LIB
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = lib().ffa_status_string(rc).decode()
+        raise FfaError(f"{what} failed: {msg} (code {rc})")
+
+
+def _shape(total_q, total_k, hq, hkv, d) -> FfaShape:
+    return FfaShape(int(total_q), int(total_k), int(hq), int(hkv), int(d))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _ranges(q_ranges, k_ranges, attn_type_map, device):
+    def conv(x, last):
+        if not isinstance(x, torch.Tensor):
+            x = torch.tensor(x, dtype=torch.int32)
+        x = x.to(device=device, dtype=torch.int32).contiguous()
+        return x.reshape(-1, 2) if last else x.reshape(-1)
+    qr, kr, ty = conv(q_ranges, True), conv(k_ranges, True), conv(attn_type_map, False)
+    if not (qr.shape[0] == kr.shape[0] == ty.shape[0]):
+        raise ValueError("q_ranges, k_ranges and attn_type_map must have the same number of slices")
+    return qr, kr, ty
+
+
+def ffa_fwd_workspace_size(total_q, total_k, num_heads_q, num_heads_kv, head_dim, n_ranges) -> int:
+    s = _shape(total_q, total_k, num_heads_q, num_heads_kv, head_dim)
+    return int(lib().ffa_fwd_workspace_size(ctypes.byref(s), int(n_ranges)))
+
+
+def ffa_bwd_workspace_size(total_q, total_k, num_heads_q, num_heads_kv, head_dim, n_ranges) -> int:
+    s = _shape(total_q, total_k, num_heads_q, num_heads_kv, head_dim)
+    return int(lib().ffa_bwd_workspace_size(ctypes.byref(s), int(n_ranges)))
+
+
+def ffa_status_string(code: int) -> str:
+    return lib().ffa_status_string(int(code)).decode()
+
+
+def ffa_set_kernel_events(fwd_start=None, fwd_stop=None, bwd_start=None, bwd_stop=None) -> None:
+    """Record torch.cuda.Event objects around the main forward / backward kernels (or stop)."""
+    h = [None if e is None else e.cuda_event for e in (fwd_start, fwd_stop, bwd_start, bwd_stop)]
+    _check(lib().ffa_set_kernel_events(*h), "ffa_set_kernel_events")
+
+
+def ffa_build_info() -> str:
+    return lib().ffa_build_info().decode()
+
+
+def ffa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_ranges, attn_type_map,
+            softmax_scale: Optional[float] = None, softcap: float = 0.0,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None
+            ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """out [Nq,Hq,d] bf16 and lse [Hq,Nq] float32 (natural log); see include/ffa.h."""
+    dev = q.device
+    nq, hq, d = q.shape
+    nk, hkv = k.shape[0], k.shape[1]
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k, "k", torch.bfloat16, dev, (nk, hkv, d))
+    _need(v, "v", torch.bfloat16, dev, (nk, hkv, d))
+    qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
+    if out is None:
+        out = torch.empty(nq, hq, d, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(hq, nq, dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev, (nq, hq, d))
+    _need(lse, "lse", torch.float32, dev, (hq, nq))
+    R = qr.shape[0]
+    shp = _shape(nq, nk, hq, hkv, d)
+    ws_bytes = int(lib().ffa_fwd_workspace_size(ctypes.byref(shp), R))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    scale = -1.0 if softmax_scale is None else float(softmax_scale)
+    rc = lib().ffa_fwd(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty), R,
+                       scale, float(softcap), _ptr(out), _ptr(lse), _ptr(workspace),
+                       workspace.numel(), _ptr(status), _stream(dev))
+    _check(rc, "ffa_fwd")
+    return out, lse
+
+
+def ffa_bwd(q, k, v, out, lse, dout, q_ranges, k_ranges, attn_type_map,
+            softmax_scale: Optional[float] = None, softcap: float = 0.0,
+            dq=None, dk=None, dv=None, workspace=None, status=None):
+    """Gradients (dq, dk, dv) of sum(out * dout); see include/ffa.h."""
+    dev = q.device
+    nq, hq, d = q.shape
+    nk, hkv = k.shape[0], k.shape[1]
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k, "k", torch.bfloat16, dev, (nk, hkv, d))
+    _need(v, "v", torch.bfloat16, dev, (nk, hkv, d))
+    _need(out, "out", torch.bfloat16, dev, (nq, hq, d))
+    _need(dout, "dout", torch.bfloat16, dev, (nq, hq, d))
+    _need(lse, "lse", torch.float32, dev, (hq, nq))
+    qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need(dq, "dq", torch.bfloat16, dev, q.shape)
+    _need(dk, "dk", torch.bfloat16, dev, k.shape)
+    _need(dv, "dv", torch.bfloat16, dev, v.shape)
+    R = qr.shape[0]
+    shp = _shape(nq, nk, hq, hkv, d)
+    ws_bytes = int(lib().ffa_bwd_workspace_size(ctypes.byref(shp), R))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    scale = -1.0 if softmax_scale is None else float(softmax_scale)
+    rc = lib().ffa_bwd(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                       _ptr(qr), _ptr(kr), _ptr(ty), R, scale, float(softcap), _ptr(dq), _ptr(dk),
+                       _ptr(dv), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    _check(rc, "ffa_bwd")
+    return dq, dk, dv
+
+
+def ffa_plan_tiles(total_q: int, total_k: int, q_ranges, k_ranges, attn_type_map, device="cuda",
+                   by_column: bool = False, num_heads_q: int = 1, num_heads_kv: int = 1,
+                   head_dim: int = 64, status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Tile classes uint8 [ceil(Nq/128), ceil(Nk/128)] computed by the device planner."""
+    dev = torch.device(device)
+    qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
+    R = qr.shape[0]
+    shp = _shape(total_q, total_k, num_heads_q, num_heads_kv, head_dim)
+    nqt, nkt = -(-int(total_q) // TILE), -(-int(total_k) // TILE)
+    tc = torch.empty(max(nqt, 0), max(nkt, 0), dtype=torch.uint8, device=dev)
+    f = lib().ffa_bwd_workspace_size if by_column else lib().ffa_fwd_workspace_size
+    ws = torch.empty(max(int(f(ctypes.byref(shp), R)), 256), dtype=torch.uint8, device=dev)
+    rc = lib().ffa_plan_tiles(ctypes.byref(shp), _ptr(qr), _ptr(kr), _ptr(ty), R, 1 if by_column else 0,
+                              _ptr(tc), _ptr(ws), ws.numel(), _ptr(status), _stream(dev))
+    _check(rc, "ffa_plan_tiles")
+    return tc
+
+
+class _FlexFlashAttn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, q_ranges, k_ranges, attn_type_map, softmax_scale, softcap):
+        out, lse = ffa_fwd(q, k, v, q_ranges, k_ranges, attn_type_map, softmax_scale, softcap)
+        ctx.save_for_backward(q, k, v, out, lse, q_ranges, k_ranges, attn_type_map)
+        ctx.softmax_scale, ctx.softcap = softmax_scale, softcap
+        return out, lse
+
+    @staticmethod
+    def backward(ctx, dout, dlse):
+        q, k, v, out, lse, qr, kr, ty = ctx.saved_tensors
+        dq, dk, dv = ffa_bwd(q, k, v, out, lse, dout.contiguous(), qr, kr, ty, ctx.softmax_scale,
+                             ctx.softcap)
+        return dq, dk, dv, None, None, None, None, None
+
+
+def flex_flash_attn_func(q, k, v, q_ranges, k_ranges, attn_type_map, max_seqlen_q=None,
+                         max_seqlen_k=None, softmax_scale=None, softcap=0.0):
+    """(out, lse) with autograd; max_seqlen_q/k are accepted and not needed (global tiling).
+
+    The gradient flows through `out` only (the lse output is treated as non-differentiable).
+    """
+    dev = q.device
+    qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
+    return _FlexFlashAttn.apply(q, k, v, qr, kr, ty, softmax_scale, softcap)

@@ -1,0 +1,696 @@
+// Backward kernels: gradients of sum(O * dO) for range-masked attention on sm_103a.
+//
+// For every visible (i, j) with P_ij = exp(x_ij - LSE_i) (recomputed from the forward LSE):
+//   dV_j += P_ij dO_i;  dP_ij = dO_i . V_j;  D_i = dO_i . O_i  (= sum_j P_ij dP_ij);
+//   dX_ij = P_ij (dP_ij - D_i);  dS = dX * (1 - tanh^2(scale q.k / softcap)) with softcap;
+//   dK_j += scale dS_ij Q_i;  dQ_i += scale dS_ij K_j.
+// The pages ask for dq/dk/dv through autograd (MagiAttention issue #180, question code:
+// out.backward(do)) without fixing the kernel; this follows the usual recomputation scheme.
+//
+// Three launches after the column planner:
+//   1. ffa_bwd_pre: D_i (fp32) and LSE_i * log2(e) padded to whole tiles, dq accumulator = 0.
+//   2. ffa_bwd_kernel: KV-stationary.  One work item = (key tile, KV head); its CTA walks the
+//      query tiles of the key tile's column list and the G query heads of the group.  Five
+//      tcgen05 GEMMs per step: S^T = K Q^T and dP^T = V dO^T (keys on TMEM lanes), then
+//      dV += P^T dO and dK += dS^T Q with P^T / dS^T read from TMEM, and dQ = dS K with dS
+//      staged in shared memory; dQ is added into the fp32 accumulator with vector atomics.
+//      dK and dV stay in TMEM for the whole item and are written once.
+//   3. ffa_bwd_dq_convert: fp32 accumulator -> bf16 dq.
+//
+// Warp roles (320 threads):
+//   warps 0-3  compute warpgroup: key row r of the tile <-> TMEM lane r; P^T, dS^T, epilogue
+//   warps 4-7  dQ warpgroup: query row r <-> TMEM lane r; drains dQ into the accumulator
+//   warp 8     TMA producer;  warp 9  MMA issuer (owns TMEM)
+// TMEM columns: S^T/P^T [0,128), dP^T/dS^T then dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
+#include <algorithm>
+
+#include "ffa_internal.h"
+#include "ffa_ptx.cuh"
+#include "../../include/ffa.h"
+
+namespace ffa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kStages = D == 128 ? 2 : 3;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kBoxBytes = kTile * 128;
+  static constexpr int kStatBytes = 2 * kTile * 4;  // LSE*log2e and D of one query tile
+  static constexpr int kK = 0;
+  static constexpr int kV = kTileBytes;
+  static constexpr int kQ = 2 * kTileBytes;                        // + s * kTileBytes
+  static constexpr int kDO = kQ + kStages * kTileBytes;            // + s * kTileBytes
+  static constexpr int kDS = kDO + kStages * kTileBytes;           // 128 keys x 128 queries bf16
+  static constexpr int kStat = kDS + kTile * kTile * 2;            // + s * kStatBytes
+  static constexpr int kBar = kStat + kStages * kStatBytes;
+  // kv_full, kv_empty, qdo_full[S], qdo_empty[S], s_full, dp_full, p_full, ds_full, dq_full,
+  // dq_empty, dkv_full, drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 8;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kMaxDyn = 232448;
+  static constexpr int kAlloc = (kTotal + 1024 <= kMaxDyn) ? kTotal + 1024 : kMaxDyn;
+  static_assert(kTotal <= kMaxDyn, "backward shared memory exceeds the per-block limit");
+};
+
+struct BwdParams {
+  int nq, nk, hq, hkv, G, nqt, nkt, n_items, qpad;
+  float scale;
+  float scale_log2;
+  float cap_c, cap_k, inv_cap_c;
+  PlanView plan;
+  const float* lse2;
+  const float* rowD;
+  float* dqacc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ int sched_item(int wave) {
+  const int c = blockIdx.x, C = gridDim.x;
+  return wave * C + ((wave & 1) ? (C - 1 - c) : c);
+}
+
+__device__ __forceinline__ void record_abort(volatile int* abort_flag, int* status) {
+  *abort_flag = 1;
+  if (status != nullptr) atomicOr(status, FFA_STATUS_TIMEOUT);
+}
+
+__device__ __forceinline__ void set_bits(uint32_t (&w)[4], int lo, int hi) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int a = max(lo - 32 * k, 0), b = min(hi - 32 * k, 32);
+    if (a < b) w[k] |= (b - a == 32) ? 0xffffffffu : (((1u << (b - a)) - 1u) << a);
+  }
+}
+
+// Mask of key row j over query tile qt: bit c set iff query qt*128+c sees key j.
+__device__ __forceinline__ void key_mask(const BwdParams& p, int cls, int j, int qt, int nsl, const int* sl,
+                                         uint32_t (&w)[4]) {
+  const int r0 = qt * kTile;
+  if (j >= p.nk) {
+    w[0] = w[1] = w[2] = w[3] = 0u;
+    return;
+  }
+  if (cls == FFA_TILE_FULL) {
+    w[0] = w[1] = w[2] = w[3] = 0xffffffffu;
+  } else {
+    w[0] = w[1] = w[2] = w[3] = 0u;
+    if (cls == FFA_TILE_PARTIAL) {
+      const int n = nsl >= 0 ? nsl : p.plan.hdr[0];
+      for (int k = 0; k < n; ++k) {
+        const int si = nsl >= 0 ? sl[k] : k;
+        const int4 s = p.plan.slices[si];
+        if (j < s.z || j >= s.w) continue;
+        const int lo = (p.plan.stypes[si] == FFA_CAUSAL) ? max(s.x, j + s.y - s.w) : s.x;
+        const int lo_c = max(lo, r0) - r0, hi_c = min(s.y, r0 + kTile) - r0;
+        if (lo_c < hi_c) set_bits(w, lo_c, hi_c);
+      }
+    }
+  }
+  const int valid = p.nq - r0;
+  if (valid < kTile) {
+    uint32_t t[4] = {0u, 0u, 0u, 0u};
+    set_bits(t, 0, valid);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] &= t[k];
+  }
+}
+
+__device__ __forceinline__ float capped_log2(float s, float cap_c, float cap_k) {
+  const float e = ex2_approx(s * cap_k);
+  return fmaf(-2.0f * cap_c, rcp_approx(1.0f + e), cap_c);
+}
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// A[m][k] K-major x B[n][k] K-major, both 128-row tiles of D columns (2 boxes when D = 128)
+template <int D>
+__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t sA, uint32_t sB, uint32_t idesc) {
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+    const uint32_t off = (s / 4) * BwdSmem<D>::kBoxBytes + (s % 4) * 32;
+    umma_ss(d_tmem, make_sdesc(sA + off, 16, 1024, kSwizzle128B), make_sdesc(sB + off, 16, 1024, kSwizzle128B),
+            idesc, s > 0 ? 1u : 0u);
+  }
+}
+
+// D (+)= A[tmem] x B where B is a 128-row (K) tile of N columns stored MN-major
+template <int N>
+__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc,
+                                        bool accumulate) {
+#pragma unroll
+  for (int s = 0; s < kTile / 16; ++s)
+    umma_ts(d_tmem, a_tmem + s * 8, make_sdesc(sB + s * 2048, kTile * 128, 1024, kSwizzle128B), idesc,
+            (accumulate || s > 0) ? 1u : 0u);
+}
+
+// dQ = dS K: A = dS^T stored [key][query] (MN-major, 2 boxes of 64 queries), B = K tile [key][d]
+template <int D>
+__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t sDS, uint32_t sK, uint32_t idesc) {
+#pragma unroll
+  for (int s = 0; s < kTile / 16; ++s)
+    umma_ss(d_tmem, make_sdesc(sDS + s * 2048, kTile * 128, 1024, kSwizzle128B),
+            make_sdesc(sK + s * 2048, kTile * 128, 1024, kSwizzle128B), idesc, s > 0 ? 1u : 0u);
+}
+
+struct BwdItem {
+  int kt, kvh, n_ent, n_steps;
+  const uint32_t* ents;
+};
+
+__device__ __forceinline__ BwdItem decode_item(const BwdParams& p, int item) {
+  BwdItem it;
+  const int rank = item / p.hkv;
+  it.kvh = item - rank * p.hkv;
+  it.kt = p.plan.col_order[rank];
+  it.n_ent = p.plan.col_cnt[it.kt];
+  it.n_steps = it.n_ent * p.G;
+  it.ents = p.plan.col_ent + static_cast<size_t>(it.kt) * p.nqt;
+  return it;
+}
+
+template <int D, bool kCap>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                   const BwdParams p) {
+  using SM = BwdSmem<D>;
+  constexpr int S = SM::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad + SM::kTotal > SM::kAlloc) {  // cannot place the swizzled tiles: report and stop
+    if (threadIdx.x == 0 && p.status != nullptr) atomicOr(p.status, FFA_STATUS_TIMEOUT);
+    return;
+  }
+  uint8_t* sm = smem_raw + pad;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::kBar);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* qdo_full = bars + 2;
+  uint64_t* qdo_empty = bars + 2 + S;
+  uint64_t* s_full = bars + 2 + 2 * S;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* ds_full = s_full + 3;
+  uint64_t* dq_full = s_full + 4;
+  uint64_t* dq_empty = s_full + 5;
+  uint64_t* dkv_full = s_full + 6;
+  uint64_t* drain = s_full + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(ds_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(dkv_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ compute warpgroup
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tbase + lane_base, tP = tbase + lane_base + 128;
+    const uint32_t tDV = tbase + lane_base + 256, tDK = tbase + lane_base + 256 + D;
+    uint8_t* sDS = sm + SM::kDS;
+    uint32_t step_cnt = 0, item_cnt = 0;
+    bool ok = true;
+    for (int wave = 0; ok; ++wave) {
+      const int item = sched_item(wave);
+      if (item >= p.n_items) break;
+      const BwdItem it = decode_item(p, item);
+      const int j = it.kt * kTile + r;  // key row
+      const bool in_keys = j < p.nk;
+      const size_t orow = (static_cast<size_t>(j) * p.hkv + it.kvh) * D;
+      if (it.n_steps == 0) {
+        if (in_keys) {
+          uint4* a = reinterpret_cast<uint4*>(p.dk + orow);
+          uint4* b = reinterpret_cast<uint4*>(p.dv + orow);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            a[c] = make_uint4(0u, 0u, 0u, 0u);
+            b[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
+      const int nsl = p.plan.col_nsl[it.kt];
+      const int* sl = p.plan.col_sl + static_cast<size_t>(it.kt) * kSliceCap;
+      for (int t = 0; t < it.n_steps && ok; ++t) {
+        const uint32_t e = it.ents[t / p.G];
+        const int qt = entry_idx(e);
+        const int cls = entry_cls(e, 0);
+        const uint32_t st = step_cnt % S;
+        const float* stat = reinterpret_cast<const float*>(sm + SM::kStat + st * SM::kStatBytes);
+        // the row statistics arrive with the stage's Q/dO (qdo_full); S^T with s_full
+        ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (step_cnt / S) & 1u, abort_flag, lim) &&
+                                         mbar_wait(s_full, step_cnt & 1u, abort_flag, lim));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t w[4];
+        const bool masked = (cls != FFA_TILE_FULL) || (qt * kTile + kTile > p.nq) || !in_keys;
+        if (masked) key_mask(p, cls, j, qt, nsl, sl, w);
+        // phase 1: P^T from S^T and the row LSEs; keep P' = P (or P (1 - tanh^2)) as bf16
+        uint32_t pp[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(tS + 32 * c, sv);
+          tmem_wait_ld();
+          reg_fence(sv);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float pv[2], pd[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int col = 32 * c + 2 * k + h2;
+              const float s = __uint_as_float(sv[2 * k + h2]);
+              const float l2 = stat[col];
+              float pr;
+              if (kCap) {
+                const float x = capped_log2(s, p.cap_c, p.cap_k);
+                pr = ex2_approx(x - l2);
+                const float th = x * p.inv_cap_c;
+                pd[h2] = pr * (1.0f - th * th);
+              } else {
+                pr = ex2_approx(fmaf(s, p.scale_log2, -l2));
+                pd[h2] = pr;
+              }
+              if (masked && !((w[col >> 5] >> (col & 31)) & 1u)) {
+                pr = 0.0f;
+                pd[h2] = 0.0f;
+              }
+              pv[h2] = pr;
+            }
+            pk[k] = pack_bf16x2(pv[0], pv[1]);
+            pp[16 * c + k] = pack_bf16x2(pd[0], pd[1]);
+          }
+          tmem_st16(tS + 16 * c, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
+        // phase 2: dS^T = P' (dP^T - D) -> TMEM (for dK) and shared memory (for dQ)
+        ok = __all_sync(0xffffffffu, mbar_wait(dp_full, step_cnt & 1u, abort_flag, lim));
+        if (ok && step_cnt > 0)  // dQ of the previous step has finished reading sDS
+          ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (step_cnt - 1) & 1u, abort_flag, lim));
+        if (!ok) break;
+        tc_fence_after();
+        const float* Drow = stat + kTile;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t dv[32];
+          tmem_ld32(tP + 32 * c, dv);
+          tmem_wait_ld();
+          reg_fence(dv);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const uint32_t pr = pp[16 * c + k];
+            const float p0 = __uint_as_float(pr << 16), p1 = __uint_as_float(pr & 0xffff0000u);
+            const int col = 32 * c + 2 * k;
+            const float d0 = p0 * (__uint_as_float(dv[2 * k]) - Drow[col]);
+            const float d1 = p1 * (__uint_as_float(dv[2 * k + 1]) - Drow[col + 1]);
+            pk[k] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tP + 16 * c, pk);
+          // shared-memory copy: row r, queries 32c..32c+31 -> half c/2, 16-byte chunks
+          // (c%2)*4 .. +3, 128-byte swizzle (chunk ^= row % 8)
+          uint8_t* rowp = sDS + (c >> 1) * (kTile * 128) + r * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int chunk = ((c & 1) * 4 + q) ^ (r & 7);
+            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+        ++step_cnt;
+      }
+      if (!ok) break;
+      // epilogue: dV and scale * dK of this key tile
+      ok = __all_sync(0xffffffffu, mbar_wait(dkv_full, item_cnt & 1u, abort_flag, lim));
+      if (!ok) break;
+      ++item_cnt;
+      tc_fence_after();
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tsrc = which ? tDK : tDV;
+        const float f = which ? p.scale : 1.0f;
+        uint4* dst = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + orow);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tsrc + 32 * c, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (in_keys) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * f, __uint_as_float(o[8 * k + 1]) * f);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * f, __uint_as_float(o[8 * k + 3]) * f);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * f, __uint_as_float(o[8 * k + 5]) * f);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * f, __uint_as_float(o[8 * k + 7]) * f);
+              dst[4 * c + k] = v;
+            }
+          }
+        }
+      }
+    }
+    if (!ok) record_abort(abort_flag, p.status);
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dQ warpgroup
+    const int q4 = warp - 4;
+    const int r = q4 * 32 + lane;
+    const uint32_t tQ = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + 128;
+    uint32_t step_cnt = 0;
+    bool ok = true;
+    for (int wave = 0; ok; ++wave) {
+      const int item = sched_item(wave);
+      if (item >= p.n_items) break;
+      const BwdItem it = decode_item(p, item);
+      for (int t = 0; t < it.n_steps; ++t) {
+        const int qt = entry_idx(it.ents[t / p.G]);
+        const int h = it.kvh * p.G + (t % p.G);
+        const int i = qt * kTile + r;
+        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, step_cnt & 1u, abort_flag, lim));
+        if (!ok) break;
+        tc_fence_after();
+        float* dst = p.dqacc + (static_cast<size_t>(i) * p.hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tQ + 32 * c, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (i < p.nq) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              red_add_v4(dst + 32 * c + 4 * k, __uint_as_float(o[4 * k]) * p.scale,
+                         __uint_as_float(o[4 * k + 1]) * p.scale, __uint_as_float(o[4 * k + 2]) * p.scale,
+                         __uint_as_float(o[4 * k + 3]) * p.scale);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        ++step_cnt;
+      }
+    }
+    if (!ok) record_abort(abort_flag, p.status);
+  } else if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t item_cnt = 0, gq = 0;
+      bool ok = true;
+      int last_use[S];
+      for (int s = 0; s < S; ++s) last_use[s] = -1;
+      int last_kv = -1;
+      for (int wave = 0; ok; ++wave) {
+        const int item = sched_item(wave);
+        if (item >= p.n_items) break;
+        const BwdItem it = decode_item(p, item);
+        if (it.n_steps == 0) continue;
+        if (item_cnt > 0) {
+          ok = mbar_wait(kv_empty, (item_cnt - 1) & 1u, abort_flag, lim);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(kv_full, 2 * SM::kTileBytes);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_2d(sm + SM::kK + b * SM::kBoxBytes, &tmK, kv_full, it.kvh * D + 64 * b, it.kt * kTile);
+          tma_load_2d(sm + SM::kV + b * SM::kBoxBytes, &tmV, kv_full, it.kvh * D + 64 * b, it.kt * kTile);
+        }
+        last_kv = static_cast<int>(item_cnt);
+        for (int t = 0; t < it.n_steps; ++t) {
+          const int qt = entry_idx(it.ents[t / p.G]);
+          const int h = it.kvh * p.G + (t % p.G);
+          const uint32_t st = gq % S, u = gq / S;
+          if (u > 0) {
+            ok = mbar_wait(&qdo_empty[st], (u - 1) & 1u, abort_flag, lim);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(&qdo_full[st], 2 * SM::kTileBytes + SM::kStatBytes);
+#pragma unroll
+          for (int b = 0; b < D / 64; ++b) {
+            tma_load_2d(sm + SM::kQ + st * SM::kTileBytes + b * SM::kBoxBytes, &tmQ, &qdo_full[st],
+                        h * D + 64 * b, qt * kTile);
+            tma_load_2d(sm + SM::kDO + st * SM::kTileBytes + b * SM::kBoxBytes, &tmDO, &qdo_full[st],
+                        h * D + 64 * b, qt * kTile);
+          }
+          const size_t so = static_cast<size_t>(h) * p.qpad + static_cast<size_t>(qt) * kTile;
+          uint8_t* sst = sm + SM::kStat + st * SM::kStatBytes;
+          bulk_load(sst, p.lse2 + so, kTile * 4, &qdo_full[st]);
+          bulk_load(sst + kTile * 4, p.rowD + so, kTile * 4, &qdo_full[st]);
+          last_use[st] = static_cast<int>(u);
+          ++gq;
+        }
+        ++item_cnt;
+      }
+      if (!ok) {
+        record_abort(abort_flag, p.status);
+        const uint64_t short_lim = 100000000ull;
+        if (last_kv >= 0) mbar_wait(kv_full, static_cast<uint32_t>(last_kv) & 1u, nullptr, short_lim);
+        for (int s = 0; s < S; ++s)
+          if (last_use[s] >= 0) mbar_wait(&qdo_full[s], static_cast<uint32_t>(last_use[s]) & 1u, nullptr, short_lim);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_st = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T: N = 128 queries
+      constexpr uint32_t idesc_acc = make_idesc_bf16(128, D, false, true);    // dV, dK: B MN-major
+      constexpr uint32_t idesc_dq = make_idesc_bf16(128, D, true, true);      // dQ: A and B MN-major
+      const uint32_t sK = smem_u32(sm + SM::kK), sV = smem_u32(sm + SM::kV);
+      const uint32_t sQ = smem_u32(sm + SM::kQ), sDO = smem_u32(sm + SM::kDO), sDS = smem_u32(sm + SM::kDS);
+      const uint32_t tS = tbase, tP = tbase + 128, tDV = tbase + 256, tDK = tbase + 256 + D;
+      uint32_t item_cnt = 0, gq = 0;
+      bool ok = true;
+      for (int wave = 0; ok; ++wave) {
+        const int item = sched_item(wave);
+        if (item >= p.n_items) break;
+        const BwdItem it = decode_item(p, item);
+        if (it.n_steps == 0) continue;
+        ok = mbar_wait(kv_full, item_cnt & 1u, abort_flag, lim);
+        if (!ok) break;
+        for (int t = 0; t < it.n_steps; ++t) {
+          const uint32_t st = gq % S;
+          ok = mbar_wait(&qdo_full[st], (gq / S) & 1u, abort_flag, lim);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t q_s = sQ + st * SM::kTileBytes, do_s = sDO + st * SM::kTileBytes;
+          issue_kmajor<D>(tS, sK, q_s, idesc_st);  // S^T = K Q^T
+          umma_commit(s_full);
+          if (gq > 0) {  // the previous dQ has been drained from the dP^T columns
+            ok = mbar_wait(dq_empty, (gq - 1) & 1u, abort_flag, lim);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          issue_kmajor<D>(tP, sV, do_s, idesc_st);  // dP^T = V dO^T
+          umma_commit(dp_full);
+          ok = mbar_wait(p_full, gq & 1u, abort_flag, lim);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts<D>(tDV, tS, do_s, idesc_acc, t > 0);  // dV += P^T dO
+          ok = mbar_wait(ds_full, gq & 1u, abort_flag, lim);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts<D>(tDK, tP, q_s, idesc_acc, t > 0);  // dK += dS^T Q
+          issue_dq<D>(tP, sDS, sK, idesc_dq);           // dQ = dS K (into the dP^T columns)
+          umma_commit(dq_full);
+          umma_commit(&qdo_empty[st]);
+          ++gq;
+        }
+        if (!ok) break;
+        umma_commit(kv_empty);
+        umma_commit(dkv_full);
+        ++item_cnt;
+      }
+      if (!ok) record_abort(abort_flag, p.status);
+      umma_commit(drain);
+      mbar_wait(drain, 0, nullptr, 100000000ull);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// D_i = dO_i . O_i and LSE_i * log2(e) per (head, row), padded to whole tiles; zero the dq
+// accumulator.  One warp per (row, head).
+template <int D>
+__global__ void __launch_bounds__(256) ffa_bwd_pre(const __nv_bfloat16* __restrict__ out,
+                                                   const __nv_bfloat16* __restrict__ dout,
+                                                   const float* __restrict__ lse, float* __restrict__ rowD,
+                                                   float* __restrict__ lse2, float* __restrict__ dqacc, int nq,
+                                                   int hq, int qpad) {
+  const int lane = threadIdx.x & 31;
+  const size_t nwarps = static_cast<size_t>(gridDim.x) * (blockDim.x >> 5);
+  const size_t total = static_cast<size_t>(qpad) * hq;
+  for (size_t wi = blockIdx.x * static_cast<size_t>(blockDim.x >> 5) + (threadIdx.x >> 5); wi < total;
+       wi += nwarps) {
+    const int h = static_cast<int>(wi / qpad);
+    const int i = static_cast<int>(wi - static_cast<size_t>(h) * qpad);
+    float dsum = 0.0f, l2 = INFINITY;
+    if (i < nq) {
+      const size_t base = (static_cast<size_t>(i) * hq + h) * D;
+      constexpr int kPer = D / 32;  // 2 or 4 elements per lane
+      const __nv_bfloat16* a = out + base + lane * kPer;
+      const __nv_bfloat16* b = dout + base + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) dsum += __bfloat162float(a[e]) * __bfloat162float(b[e]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+      float* z = dqacc + base + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) z[e] = 0.0f;
+      const float l = lse[static_cast<size_t>(h) * nq + i];
+      l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+    }
+    if (lane == 0) {
+      rowD[wi] = i < nq ? dsum : 0.0f;
+      lse2[wi] = l2;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) ffa_bwd_dq_convert(const float* __restrict__ acc,
+                                                          __nv_bfloat16* __restrict__ dq, size_t n) {
+  const size_t n4 = n / 4;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    reinterpret_cast<uint2*>(dq)[i] = o;
+  }
+}
+
+template <int D, bool kCap>
+cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
+  using SM = BwdSmem<D>;
+  static bool attr_set = false;
+  auto kern = ffa_bwd_kernel<D, kCap>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const auto& P = a.P;
+  const int qpad = P.nqt * kTile;
+  const int nsm = num_sms();
+  {
+    const size_t warps = static_cast<size_t>(qpad) * P.hq;
+    const int blocks = static_cast<int>(std::min<size_t>((warps + 7) / 8, static_cast<size_t>(nsm) * 16));
+    ffa_bwd_pre<D><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(a.out),
+                                                static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.rowD, a.lse2,
+                                                a.dqacc, P.nq, P.hq, qpad);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_tile_map(&mq, a.q, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile) ||
+      !encode_tile_map(&mdo, a.dout, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile) ||
+      !encode_tile_map(&mk, a.k, static_cast<uint64_t>(P.hkv) * D, P.nk, 64, kTile) ||
+      !encode_tile_map(&mv, a.v, static_cast<uint64_t>(P.hkv) * D, P.nk, 64, kTile))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  p.nq = P.nq; p.nk = P.nk; p.hq = P.hq; p.hkv = P.hkv; p.G = P.hq / P.hkv;
+  p.nqt = P.nqt; p.nkt = P.nkt;
+  p.n_items = P.nkt * P.hkv;
+  p.qpad = qpad;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  p.cap_c = a.softcap * kLog2e;
+  p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
+  p.inv_cap_c = a.softcap > 0.0f ? 1.0f / p.cap_c : 0.0f;
+  p.plan = a.plan;
+  p.lse2 = a.lse2;
+  p.rowD = a.rowD;
+  p.dqacc = a.dqacc;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.status = a.status;
+  p.wait_limit_ns = a.wait_limit_ns;
+  const int grid = p.n_items < nsm ? p.n_items : nsm;
+  if (grid > 0) {
+    if (g_kernel_events.bwd_start != nullptr) cudaEventRecord(g_kernel_events.bwd_start, stream);
+    kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, mdo, p);
+    if (g_kernel_events.bwd_stop != nullptr) cudaEventRecord(g_kernel_events.bwd_stop, stream);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const size_t n = static_cast<size_t>(P.nq) * P.hq * D;
+  const int blocks = static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, static_cast<size_t>(nsm) * 8));
+  if (blocks > 0) ffa_bwd_dq_convert<<<blocks, 256, 0, stream>>>(a.dqacc, static_cast<__nv_bfloat16*>(a.dq), n);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s) {
+  const bool cap = a.softcap > 0.0f;
+  if (a.P.d == 64) return cap ? launch_impl<64, true>(a, s) : launch_impl<64, false>(a, s);
+  return cap ? launch_impl<128, true>(a, s) : launch_impl<128, false>(a, s);
+}
+
+}  // namespace ffa

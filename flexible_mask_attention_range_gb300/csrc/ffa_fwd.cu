@@ -1,0 +1,546 @@
+// Forward kernel: fused range-masked softmax attention on sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes: for every query row i and head h, over the keys j visible to i under
+// the union of the slices, O_i = sum_j softmax_j(x_ij) v_j and LSE_i = log sum_j e^{x_ij},
+// with x = scale * q.k, or softcap * tanh(scale * q.k / softcap) when softcap > 0.  The
+// interface is flex_flash_attn_func's (MagiAttention issue #180); the mask is applied by
+// zeroing P where a pair is not visible, with no padding and no per-sequence descriptor
+// edits, because the slice ranges index the flat packed tensors directly ("Questions about
+// ex77 blackwell Flash attention", CUTLASS issue #2192: masking P during softmax instead of
+// tensormap.replace or front padding).  Fully masked tiles are skipped and fully visible
+// tiles skip the element mask (Flex Attention paper, section 4, "Full Block Optimization");
+// later K/V tiles are prefetched while the current one is processed (same section, "Data
+// Prefetching Pipeline").
+//
+// CTA = one work item = two 128-row query tiles sharing one K/V stream: either two query
+// heads of one GQA group over the same query tile (G even) or two adjacent query tiles of
+// one head (G odd).  Persistent grid (one CTA per SM), static longest-first snake schedule.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax warpgroup 0: row r of query tile 0 <-> TMEM lane r
+//   warps 4-7  softmax warpgroup 1: query tile 1
+//   warp 8     TMA producer (lane 0): Q tiles once per item, K/V tiles through a ring
+//   warp 9     MMA issuer (lane 0): S_t = Q_t K^T into TMEM, O_t += P_t V with P_t read
+//              from TMEM; owns the TMEM allocation
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).  P_t is
+// written as bf16 over the first 64 columns of S_t.
+//
+// Online softmax in the log2 domain with a lazily updated reference max: the reference m
+// of a row moves only when a new tile's max exceeds it by more than kTau (p <= 2^kTau), and
+// only then is that row of O rescaled in TMEM.  Rows with no visible key so far use 0 as
+// the reference (safe softmax), so fully masked rows end with l = 0: O = 0, LSE = -inf.
+#include "ffa_internal.h"
+#include "ffa_ptx.cuh"
+#include "../../include/ffa.h"
+
+namespace ffa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kTau = 8.0f;
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kTileBytes = kTile * D * 2;  // 128 rows x D bf16
+  static constexpr int kBoxBytes = kTile * 128;     // 128 rows x 64 bf16 (one TMA box)
+  static constexpr int kQ0 = 0;
+  static constexpr int kQ1 = kTileBytes;
+  static constexpr int kK = 2 * kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kBar = kV + kStages * kTileBytes;
+  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain
+  static constexpr int kNumBars = 2 + 3 * kStages + 7;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kAlloc = kTotal + 1024;
+};
+
+struct FwdParams {
+  int nq, nk, hq, hkv, G, nqt, nkt;
+  int head_pair, slots, n_items;
+  float scale_log2;  // softmax_scale * log2(e)
+  float cap_c;       // softcap * log2(e)
+  float cap_k;       // 2 * softmax_scale * log2(e) / softcap
+  PlanView plan;
+  __nv_bfloat16* out;
+  float* lse;
+  int* status;
+  uint64_t wait_limit_ns;
+};
+
+struct Item {
+  int g, qt0, qt1, h0, h1, kvh;
+};
+
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int item) {
+  Item it;
+  const int rank = item / p.slots, slot = item - rank * p.slots;
+  it.g = p.plan.grp_order[rank];
+  if (p.head_pair) {
+    it.qt0 = it.qt1 = it.g;
+    it.h0 = 2 * slot;
+    it.h1 = 2 * slot + 1;
+  } else {
+    it.qt0 = 2 * it.g;
+    it.qt1 = 2 * it.g + 1;
+    it.h0 = it.h1 = slot;
+  }
+  it.kvh = it.h0 / p.G;
+  return it;
+}
+
+// Static snake schedule over the longest-first item order.
+__device__ __forceinline__ int sched_item(int wave) {
+  const int c = blockIdx.x, C = gridDim.x;
+  return wave * C + ((wave & 1) ? (C - 1 - c) : c);
+}
+
+__device__ __forceinline__ void record_abort(volatile int* abort_flag, int* status) {
+  *abort_flag = 1;
+  if (status != nullptr) atomicOr(status, FFA_STATUS_TIMEOUT);
+}
+
+// bits [lo, hi) of a 128-bit row mask, lo/hi relative to the tile
+__device__ __forceinline__ void set_bits(uint32_t (&w)[4], int lo, int hi) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int a = max(lo - 32 * k, 0), b = min(hi - 32 * k, 32);
+    if (a < b) w[k] |= (b - a == 32) ? 0xffffffffu : (((1u << (b - a)) - 1u) << a);
+  }
+}
+
+// Element mask of query row `row` over key tile kt: bit c set iff key kt*128+c is visible.
+__device__ __forceinline__ void row_mask(const FwdParams& p, int cls, int row, int kt, int nsl, const int* sl,
+                                         uint32_t (&w)[4]) {
+  const int c0 = kt * kTile;
+  if (cls == FFA_TILE_FULL) {
+    w[0] = w[1] = w[2] = w[3] = 0xffffffffu;
+  } else {
+    w[0] = w[1] = w[2] = w[3] = 0u;
+    if (cls == FFA_TILE_PARTIAL) {
+      const int n = nsl >= 0 ? nsl : p.plan.hdr[0];
+      for (int k = 0; k < n; ++k) {
+        const int si = nsl >= 0 ? sl[k] : k;
+        const int4 s = p.plan.slices[si];
+        if (row < s.x || row >= s.y) continue;
+        const int hi = (p.plan.stypes[si] == FFA_CAUSAL) ? min(s.w, row + s.w - s.y + 1) : s.w;
+        const int lo_c = max(s.z, c0) - c0, hi_c = min(hi, c0 + kTile) - c0;
+        if (lo_c < hi_c) set_bits(w, lo_c, hi_c);
+      }
+    }
+  }
+  const int valid = p.nk - c0;  // keys beyond Nk are never visible
+  if (valid < kTile) {
+    uint32_t t[4] = {0u, 0u, 0u, 0u};
+    set_bits(t, 0, valid);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] &= t[k];
+  }
+}
+
+// tanh(y) * C in the log2 domain from one exp2 and one reciprocal:
+// tanh(y) = 1 - 2 / (1 + e^{2y}); e^{2y} = 2^{s * cap_k}.
+__device__ __forceinline__ float capped_log2(float s, float cap_c, float cap_k) {
+  const float e = ex2_approx(s * cap_k);
+  return fmaf(-2.0f * cap_c, rcp_approx(1.0f + e), cap_c);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sQ, uint32_t sK, uint32_t idesc) {
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+    const uint32_t off = (s / 4) * FwdSmem<D>::kBoxBytes + (s % 4) * 32;
+    umma_ss(d_tmem, make_sdesc(sQ + off, 16, 1024, kSwizzle128B), make_sdesc(sK + off, 16, 1024, kSwizzle128B),
+            idesc, s > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint32_t sV, uint32_t idesc,
+                                        bool accumulate) {
+#pragma unroll
+  for (int s = 0; s < kTile / 16; ++s) {
+    umma_ts(d_tmem, a_tmem + s * 8, make_sdesc(sV + s * 2048, FwdSmem<D>::kBoxBytes, 1024, kSwizzle128B), idesc,
+            (accumulate || s > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, bool kCap>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using SM = FwdSmem<D>;
+  constexpr int S = SM::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* sm = smem_raw + pad;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::kBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* v_full = bars + 2 + S;
+  uint64_t* kv_empty = bars + 2 + 2 * S;
+  uint64_t* s_full = bars + 2 + 3 * S;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = s_full + 4;
+  uint64_t* drain = s_full + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_full[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int wg = warp >> 2, q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tbase + lane_base + wg * 128;
+    const uint32_t tO = tbase + lane_base + 256 + wg * D;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    for (int wave = 0; ok; ++wave) {
+      const int item = sched_item(wave);
+      if (item >= p.n_items) break;
+      const Item it = decode_item(p, item);
+      const int n = p.plan.grp_cnt[it.g];
+      const int qt = wg ? it.qt1 : it.qt0;
+      const int h = wg ? it.h1 : it.h0;
+      const int row = qt * kTile + r;
+      const bool in_rows = row < p.nq;
+      if (n == 0) {
+        if (in_rows) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
+        }
+        continue;
+      }
+      const uint32_t* ents = p.plan.grp_ent + static_cast<size_t>(it.g) * p.nkt;
+      const int nsl = qt < p.nqt ? p.plan.row_nsl[qt] : 0;
+      const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
+      float m_run = -INFINITY, l_run = 0.0f;
+      for (int j = 0; j < n; ++j) {
+        const uint32_t e = ents[j];
+        const int kt = entry_idx(e);
+        const int cls = entry_cls(e, wg);
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], s_cnt & 1u, abort_flag, lim));
+        if (!ok) break;
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sv[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence(sv[c]);
+        const bool masked = (cls != FFA_TILE_FULL) || (kt * kTile + kTile > p.nk);
+        float mx = -INFINITY;
+        if (masked) {
+          uint32_t w[4];
+          row_mask(p, cls, row, kt, nsl, sl, w);
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            float x = __uint_as_float(sv[c >> 5][c & 31]);
+            if (kCap) x = capped_log2(x, p.cap_c, p.cap_k);
+            x = ((w[c >> 5] >> (c & 31)) & 1u) ? x : -INFINITY;
+            sv[c >> 5][c & 31] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            float x = __uint_as_float(sv[c >> 5][c & 31]);
+            if (kCap) {
+              x = capped_log2(x, p.cap_c, p.cap_k);
+              sv[c >> 5][c & 31] = __float_as_uint(x);
+            }
+            mx = fmaxf(mx, x);
+          }
+        }
+        const float m_tile = kCap ? mx : mx * p.scale_log2;
+        const bool need = m_tile > m_run + kTau;
+        const bool rescale = need && (m_run != -INFINITY);
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float alpha = rescale ? ex2_approx(m_run - m_tile) : 1.0f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(tO + 32 * c, o);
+          }
+          tmem_wait_st();
+          if (rescale) l_run *= alpha;
+        }
+        if (need) m_run = m_tile;
+        const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
+        float sum = 0.0f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float x0 = __uint_as_float(sv[c4][2 * k]), x1 = __uint_as_float(sv[c4][2 * k + 1]);
+            const float p0 = kCap ? ex2_approx(x0 + neg_m) : ex2_approx(fmaf(x0, p.scale_log2, neg_m));
+            const float p1 = kCap ? ex2_approx(x1 + neg_m) : ex2_approx(fmaf(x1, p.scale_log2, neg_m));
+            sum += p0 + p1;
+            pk[k] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + 16 * c4, pk);
+        }
+        l_run += sum;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[wg]);
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, LSE
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_full[wg], o_cnt & 1u, abort_flag, lim));
+      if (!ok) break;
+      ++o_cnt;
+      tc_fence_after();
+      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        if (in_rows) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+            dst[4 * c + k] = v;
+          }
+        }
+      }
+      if (in_rows)
+        p.lse[static_cast<size_t>(h) * p.nq + row] = l_run > 0.0f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
+    }
+    if (!ok) record_abort(abort_flag, p.status);
+  } else if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it_cnt = 0;
+      uint32_t gk = 0;
+      bool ok = true;
+      int last_use[S];
+      for (int s = 0; s < S; ++s) last_use[s] = -1;
+      for (int wave = 0; ok; ++wave) {
+        const int item = sched_item(wave);
+        if (item >= p.n_items) break;
+        const Item it = decode_item(p, item);
+        const int n = p.plan.grp_cnt[it.g];
+        if (n == 0) continue;
+        if (it_cnt > 0) {
+          ok = mbar_wait(q_empty, (it_cnt - 1) & 1u, abort_flag, lim);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(q_full, 2 * SM::kTileBytes);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_2d(sm + SM::kQ0 + b * SM::kBoxBytes, &tmQ, q_full, it.h0 * D + 64 * b, it.qt0 * kTile);
+          tma_load_2d(sm + SM::kQ1 + b * SM::kBoxBytes, &tmQ, q_full, it.h1 * D + 64 * b, it.qt1 * kTile);
+        }
+        const uint32_t* ents = p.plan.grp_ent + static_cast<size_t>(it.g) * p.nkt;
+        for (int j = 0; j < n; ++j) {
+          const int kt = entry_idx(ents[j]);
+          const uint32_t st = gk % S, u = gk / S;
+          if (u > 0) {
+            ok = mbar_wait(&kv_empty[st], (u - 1) & 1u, abort_flag, lim);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(&k_full[st], SM::kTileBytes);
+#pragma unroll
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_2d(sm + SM::kK + st * SM::kTileBytes + b * SM::kBoxBytes, &tmK, &k_full[st],
+                        it.kvh * D + 64 * b, kt * kTile);
+          mbar_arrive_expect_tx(&v_full[st], SM::kTileBytes);
+#pragma unroll
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_2d(sm + SM::kV + st * SM::kTileBytes + b * SM::kBoxBytes, &tmV, &v_full[st],
+                        it.kvh * D + 64 * b, kt * kTile);
+          last_use[st] = static_cast<int>(u);
+          ++gk;
+        }
+        ++it_cnt;
+      }
+      if (!ok) {
+        record_abort(abort_flag, p.status);
+        // let the copies already issued land before the CTA's shared memory is released
+        const uint64_t short_lim = 100000000ull;
+        if (it_cnt > 0 || gk > 0) mbar_wait(q_full, (it_cnt - (gk > 0 && it_cnt == 0 ? 0 : 0)) & 1u, nullptr, 0);
+        for (int s = 0; s < S; ++s) {
+          if (last_use[s] < 0) continue;
+          mbar_wait(&k_full[s], static_cast<uint32_t>(last_use[s]) & 1u, nullptr, short_lim);
+          mbar_wait(&v_full[s], static_cast<uint32_t>(last_use[s]) & 1u, nullptr, short_lim);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, D, false, true);
+      const uint32_t sQ0 = smem_u32(sm + SM::kQ0), sQ1 = smem_u32(sm + SM::kQ1);
+      const uint32_t sK = smem_u32(sm + SM::kK), sV = smem_u32(sm + SM::kV);
+      const uint32_t tS0 = tbase, tS1 = tbase + 128, tO0 = tbase + 256, tO1 = tbase + 256 + D;
+      uint32_t it_cnt = 0, gk = 0, pc0 = 0, pc1 = 0;
+      bool ok = true;
+      for (int wave = 0; ok; ++wave) {
+        const int item = sched_item(wave);
+        if (item >= p.n_items) break;
+        const Item it = decode_item(p, item);
+        const int n = p.plan.grp_cnt[it.g];
+        if (n == 0) continue;
+        ok = mbar_wait(q_full, it_cnt & 1u, abort_flag, lim);
+        if (!ok) break;
+        {
+          const uint32_t st = gk % S;
+          ok = mbar_wait(&k_full[st], (gk / S) & 1u, abort_flag, lim);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk<D>(tS0, sQ0, sK + st * SM::kTileBytes, idesc_qk);
+          umma_commit(&s_full[0]);
+          issue_qk<D>(tS1, sQ1, sK + st * SM::kTileBytes, idesc_qk);
+          umma_commit(&s_full[1]);
+          if (n == 1) umma_commit(q_empty);
+        }
+        for (int j = 0; j < n && ok; ++j) {
+          const uint32_t g = gk + j, st = g % S;
+          ok = mbar_wait(&v_full[st], (g / S) & 1u, abort_flag, lim) &&
+               mbar_wait(&p_full[0], pc0 & 1u, abort_flag, lim);
+          if (!ok) break;
+          ++pc0;
+          tc_fence_after();
+          issue_pv<D>(tO0, tS0, sV + st * SM::kTileBytes, idesc_pv, j > 0);
+          if (j == n - 1) umma_commit(&o_full[0]);
+          const uint32_t g1 = g + 1, st1 = g1 % S;
+          if (j + 1 < n) {
+            ok = mbar_wait(&k_full[st1], (g1 / S) & 1u, abort_flag, lim);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk<D>(tS0, sQ0, sK + st1 * SM::kTileBytes, idesc_qk);
+            umma_commit(&s_full[0]);
+          }
+          ok = mbar_wait(&p_full[1], pc1 & 1u, abort_flag, lim);
+          if (!ok) break;
+          ++pc1;
+          tc_fence_after();
+          issue_pv<D>(tO1, tS1, sV + st * SM::kTileBytes, idesc_pv, j > 0);
+          umma_commit(&kv_empty[st]);
+          if (j == n - 1) umma_commit(&o_full[1]);
+          if (j + 1 < n) {
+            issue_qk<D>(tS1, sQ1, sK + st1 * SM::kTileBytes, idesc_qk);
+            umma_commit(&s_full[1]);
+            if (j + 2 == n) umma_commit(q_empty);
+          }
+        }
+        gk += n;
+        ++it_cnt;
+      }
+      if (!ok) record_abort(abort_flag, p.status);
+      // every MMA issued by this thread has completed once `drain` fires
+      umma_commit(drain);
+      mbar_wait(drain, 0, nullptr, 100000000ull);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool kCap>
+cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
+  using SM = FwdSmem<D>;
+  static bool attr_set = false;
+  auto kern = ffa_fwd_kernel<D, kCap>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap mq, mk, mv;
+  const auto& P = a.P;
+  if (!encode_tile_map(&mq, a.q, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile) ||
+      !encode_tile_map(&mk, a.k, static_cast<uint64_t>(P.hkv) * D, P.nk, 64, kTile) ||
+      !encode_tile_map(&mv, a.v, static_cast<uint64_t>(P.hkv) * D, P.nk, 64, kTile))
+    return cudaErrorInvalidValue;
+  FwdParams p;
+  p.nq = P.nq; p.nk = P.nk; p.hq = P.hq; p.hkv = P.hkv; p.G = P.hq / P.hkv;
+  p.nqt = P.nqt; p.nkt = P.nkt;
+  p.head_pair = a.head_pair; p.slots = a.slots; p.n_items = a.n_items;
+  p.scale_log2 = a.scale * kLog2e;
+  p.cap_c = a.softcap * kLog2e;
+  p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
+  p.plan = a.plan;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.status = a.status;
+  p.wait_limit_ns = a.wait_limit_ns;
+  const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
+  if (grid <= 0) return cudaSuccess;
+  if (g_kernel_events.fwd_start != nullptr) cudaEventRecord(g_kernel_events.fwd_start, stream);
+  kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, p);
+  if (g_kernel_events.fwd_stop != nullptr) cudaEventRecord(g_kernel_events.fwd_stop, stream);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
+  const bool cap = a.softcap > 0.0f;
+  if (a.P.d == 64) return cap ? launch_impl<64, true>(a, s) : launch_impl<64, false>(a, s);
+  return cap ? launch_impl<128, true>(a, s) : launch_impl<128, false>(a, s);
+}
+
+}  // namespace ffa

@@ -1,0 +1,169 @@
+// Internal structures shared by the host entry points and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace ffa {
+
+constexpr int kTile = 128;         // global tile edge (query rows and key columns)
+constexpr int kSliceCap = 64;      // slice ids stored per tile row / tile column for masks
+constexpr int kSliceSmem = 512;    // slices staged in shared memory by the planner
+constexpr int kMaxTiles = 8192;    // ceil(FFA_MAX_TOKENS / 128)
+
+// Entry of a work list: key-tile (or query-tile) index in bits 0..23, class of sub-tile a
+// in bits 24..25 and of sub-tile b in bits 26..27.
+__host__ __device__ inline uint32_t make_entry(int idx, int ca, int cb) {
+  return static_cast<uint32_t>(idx) | (static_cast<uint32_t>(ca) << 24) | (static_cast<uint32_t>(cb) << 26);
+}
+__host__ __device__ inline int entry_idx(uint32_t e) { return static_cast<int>(e & 0xFFFFFFu); }
+__host__ __device__ inline int entry_cls(uint32_t e, int sub) { return static_cast<int>((e >> (24 + 2 * sub)) & 3u); }
+
+// Workspace layout.  Every region starts on a 256-byte boundary.
+struct WsLayout {
+  int64_t nq = 0, nk = 0;
+  int hq = 0, hkv = 0, d = 0, R = 0;
+  int nqt = 0, nkt = 0;
+  bool head_pair = true;  // forward pairs two query heads of one KV group (else two q-tiles)
+  int ngrp = 0, slots = 0;
+  size_t hdr = 0, slices = 0, stypes = 0, cls = 0;
+  size_t row_nsl = 0, row_sl = 0, grp_cnt = 0, grp_ent = 0, grp_order = 0;
+  size_t col_nsl = 0, col_sl = 0, col_cnt = 0, col_ent = 0, col_order = 0;
+  size_t rowD = 0, lse2 = 0, dqacc = 0;
+  size_t fwd_total = 0, bwd_total = 0;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int R) {
+  WsLayout L;
+  L.nq = nq; L.nk = nk; L.hq = hq; L.hkv = hkv; L.d = d; L.R = R;
+  L.nqt = static_cast<int>((nq + kTile - 1) / kTile);
+  L.nkt = static_cast<int>((nk + kTile - 1) / kTile);
+  const int G = hkv > 0 ? hq / hkv : 1;
+  L.head_pair = (G % 2 == 0);
+  L.ngrp = L.head_pair ? L.nqt : (L.nqt + 1) / 2;
+  L.slots = L.head_pair ? hq / 2 : hq;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+  const size_t Rn = static_cast<size_t>(R > 0 ? R : 1);
+  const size_t nqt = static_cast<size_t>(L.nqt > 0 ? L.nqt : 1), nkt = static_cast<size_t>(L.nkt > 0 ? L.nkt : 1);
+  const size_t ngrp = static_cast<size_t>(L.ngrp > 0 ? L.ngrp : 1);
+  L.hdr = take(64);
+  L.slices = take(Rn * 16);
+  L.stypes = take(Rn * 4);
+  L.cls = take(nqt * nkt);
+  const size_t common = o;
+  L.row_nsl = take(nqt * 4);
+  L.row_sl = take(nqt * kSliceCap * 4);
+  L.grp_cnt = take(ngrp * 4);
+  L.grp_ent = take(ngrp * nkt * 4);
+  L.grp_order = take(ngrp * 4);
+  L.fwd_total = o;
+  o = common;
+  L.col_nsl = take(nkt * 4);
+  L.col_sl = take(nkt * kSliceCap * 4);
+  L.col_cnt = take(nkt * 4);
+  L.col_ent = take(nkt * nqt * 4);
+  L.col_order = take(nkt * 4);
+  // per-row statistics padded to whole tiles: [Hq, nqt * 128]
+  L.rowD = take(static_cast<size_t>(hq) * nqt * kTile * 4);
+  L.lse2 = take(static_cast<size_t>(hq) * nqt * kTile * 4);
+  L.dqacc = take(static_cast<size_t>(nq > 0 ? nq : 1) * hq * d * 4);
+  L.bwd_total = o;
+  return L;
+}
+
+// Device-side view of the planner's output.
+struct PlanView {
+  int* hdr;              // [0] = number of valid slices
+  int4* slices;          // (qs, qe, ks, ke) of valid, non-empty slices, input order
+  int* stypes;           // type of each
+  uint8_t* cls;          // [nqt, nkt]
+  int* row_nsl;          // per query tile: number of slices touching it, -1 if > kSliceCap
+  int* row_sl;           // [nqt, kSliceCap]
+  int* grp_cnt;          // per forward group: number of work-list entries
+  uint32_t* grp_ent;     // [ngrp, nkt]
+  int* grp_order;        // groups, longest list first
+  int* col_nsl;          // per key tile: number of slices touching it, -1 if > kSliceCap
+  int* col_sl;           // [nkt, kSliceCap]
+  int* col_cnt;
+  uint32_t* col_ent;     // [nkt, nqt]
+  int* col_order;
+};
+
+inline PlanView plan_view(const WsLayout& L, void* ws) {
+  char* b = static_cast<char*>(ws);
+  PlanView v;
+  v.hdr = reinterpret_cast<int*>(b + L.hdr);
+  v.slices = reinterpret_cast<int4*>(b + L.slices);
+  v.stypes = reinterpret_cast<int*>(b + L.stypes);
+  v.cls = reinterpret_cast<uint8_t*>(b + L.cls);
+  v.row_nsl = reinterpret_cast<int*>(b + L.row_nsl);
+  v.row_sl = reinterpret_cast<int*>(b + L.row_sl);
+  v.grp_cnt = reinterpret_cast<int*>(b + L.grp_cnt);
+  v.grp_ent = reinterpret_cast<uint32_t*>(b + L.grp_ent);
+  v.grp_order = reinterpret_cast<int*>(b + L.grp_order);
+  v.col_nsl = reinterpret_cast<int*>(b + L.col_nsl);
+  v.col_sl = reinterpret_cast<int*>(b + L.col_sl);
+  v.col_cnt = reinterpret_cast<int*>(b + L.col_cnt);
+  v.col_ent = reinterpret_cast<uint32_t*>(b + L.col_ent);
+  v.col_order = reinterpret_cast<int*>(b + L.col_order);
+  return v;
+}
+
+struct ProblemDims {
+  int nq, nk, hq, hkv, d, nqt, nkt;
+};
+
+// Planner launches (ffa_plan.cu).  Each returns a cudaError_t of the launches.
+cudaError_t launch_plan_slices(const ProblemDims& P, const int32_t* q_ranges, const int32_t* k_ranges,
+                               const int32_t* types, int R, const PlanView& v, int32_t* status, cudaStream_t s);
+cudaError_t launch_plan_rows(const ProblemDims& P, const WsLayout& L, const PlanView& v, cudaStream_t s);
+cudaError_t launch_plan_cols(const ProblemDims& P, const PlanView& v, cudaStream_t s);
+
+// Forward (ffa_fwd.cu)
+struct FwdArgs {
+  ProblemDims P;
+  int head_pair, ngrp, slots, n_items;
+  float scale, softcap;
+  const void *q, *k, *v;
+  void* out;
+  float* lse;
+  PlanView plan;
+  int32_t* status;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
+
+// Backward (ffa_bwd.cu)
+struct BwdArgs {
+  ProblemDims P;
+  float scale, softcap;
+  const void *q, *k, *v, *out, *dout;
+  const float* lse;
+  void *dq, *dk, *dv;
+  float* rowD;   // D_i = dO_i . O_i, [Hq, nqt*128], 0 beyond Nq
+  float* lse2;   // LSE_i * log2(e), [Hq, nqt*128], +inf for empty rows and beyond Nq
+  float* dqacc;  // float32 [Nq, Hq, d]
+  PlanView plan;
+  int32_t* status;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
+
+// Optional events recorded around the main kernels (ffa_api.cu)
+struct KernelEvents {
+  cudaEvent_t fwd_start = nullptr, fwd_stop = nullptr, bwd_start = nullptr, bwd_stop = nullptr;
+};
+extern KernelEvents g_kernel_events;
+
+// TMA descriptor creation (ffa_api.cu)
+bool encode_tile_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                     uint32_t box_rows);
+int num_sms();
+
+}  // namespace ffa

@@ -1,0 +1,322 @@
+// Range-to-tile planner.
+//
+// Turns the slice list (q_range, k_range, FULL|CAUSAL) into the data the attention kernels
+// walk: the class of every tile of the global 128 x 128 grid (EMPTY / PARTIAL / FULL, the
+// block classification of the Flex Attention paper, section 4, "Block Sparsity" and "Full
+// Block Optimization"), per-row (forward) and per-column (backward) lists of the non-empty
+// tiles with their classes (the paper's non-masked block counts and indices), the slices
+// that touch each tile row / column (used to rebuild the element mask of PARTIAL tiles),
+// and a longest-first order of the lists for load balance.  Zero-area slices (start == end
+// in either range) are dropped first and cost nothing afterwards (MagiAttention issue #180,
+// maintainer reply: the tile scheduler skips empty ranges).
+//
+// Visibility of (i, j) under slice [qs,qe) x [ks,ke): qs <= i < qe, ks <= j < ke and, for
+// CAUSAL, j <= i + ke - qe (bottom-right alignment).  Several slices combine by OR.
+#include "ffa_internal.h"
+#include "../../include/ffa.h"
+
+namespace ffa {
+namespace {
+
+__device__ int block_exclusive_scan(int v, int* warp_buf, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_buf[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = lane < nw ? warp_buf[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_buf[lane] = s;
+  }
+  __syncthreads();
+  const int excl = x - v + (w > 0 ? warp_buf[w - 1] : 0);
+  *total = warp_buf[nw - 1];
+  __syncthreads();
+  return excl;
+}
+
+// ---------------------------------------------------------------- 1. slice filter
+// One block: validate, drop zero-area slices, compact the rest in input order.
+__global__ void __launch_bounds__(1024) plan_slices_kernel(const int32_t* __restrict__ qr,
+                                                           const int32_t* __restrict__ kr,
+                                                           const int32_t* __restrict__ ty, int R, int nq, int nk,
+                                                           PlanView v, int32_t* status) {
+  __shared__ int warp_buf[32];
+  int base = 0, bad = 0;
+  for (int c = 0; c < R; c += blockDim.x) {
+    const int r = c + threadIdx.x;
+    int keep = 0;
+    int4 s = make_int4(0, 0, 0, 0);
+    int t = 0;
+    if (r < R) {
+      s = make_int4(qr[2 * r], qr[2 * r + 1], kr[2 * r], kr[2 * r + 1]);
+      t = ty[r];
+      const bool ok = 0 <= s.x && s.x <= s.y && s.y <= nq && 0 <= s.z && s.z <= s.w && s.w <= nk &&
+                      (t == FFA_FULL || t == FFA_CAUSAL);
+      if (!ok) bad = 1;
+      keep = ok && s.x < s.y && s.z < s.w;
+    }
+    int total;
+    const int pos = block_exclusive_scan(keep, warp_buf, &total);
+    if (keep) {
+      v.slices[base + pos] = s;
+      v.stypes[base + pos] = t;
+    }
+    base += total;
+  }
+  if (bad && status != nullptr) atomicOr(status, FFA_STATUS_BAD_RANGE);
+  if (threadIdx.x == 0) v.hdr[0] = base;
+}
+
+// ---------------------------------------------------------------- tile classification
+// Is any pair of rows [r0,r1) x columns [c0,c1) visible under slice s?
+__device__ __forceinline__ bool slice_touches(int4 s, int t, int r0, int r1, int c0, int c1) {
+  const int a = max(s.x, r0), b = min(s.y, r1);
+  if (a >= b) return false;
+  const int hi_last = (t == FFA_CAUSAL) ? min(s.w, (b - 1) + s.w - s.y + 1) : s.w;
+  return max(s.z, c0) < min(hi_last, c1);
+}
+// Is every pair of rows [r0,r1) x columns [c0,c1) visible under slice s alone?
+__device__ __forceinline__ bool slice_covers(int4 s, int t, int r0, int r1, int c0, int c1) {
+  if (s.x > r0 || s.y < r1 || s.z > c0) return false;
+  const int hi_first = (t == FFA_CAUSAL) ? min(s.w, r0 + s.w - s.y + 1) : s.w;
+  return hi_first >= c1;
+}
+
+// Slice list access: either staged in shared memory or read from the global compact list
+// (when more slices touch the row/column than fit in shared memory).
+struct SliceList {
+  const int4* s;
+  const int* t;
+  int n;
+};
+
+// Class of the tile rows [r0,r1) x columns [c0,c1) under the union of the slices in `L`
+// (which must contain every slice that touches the tile).
+__device__ int classify_tile(const SliceList& L, int r0, int r1, int c0, int c1) {
+  int n_touch = 0;
+  for (int i = 0; i < L.n; ++i) {
+    const int4 s = L.s[i];
+    const int t = L.t[i];
+    if (!slice_touches(s, t, r0, r1, c0, c1)) continue;
+    if (slice_covers(s, t, r0, r1, c0, c1)) return FFA_TILE_FULL;
+    ++n_touch;
+  }
+  if (n_touch == 0) return FFA_TILE_EMPTY;
+  if (n_touch == 1) return FFA_TILE_PARTIAL;
+  // Several slices touch the tile and none covers it alone: check, row by row, whether the
+  // union of their visible intervals covers [c0, c1).
+  for (int i = r0; i < r1; ++i) {
+    int cur = c0;
+    bool progressed = true;
+    while (cur < c1 && progressed) {
+      progressed = false;
+      for (int k = 0; k < L.n; ++k) {
+        const int4 s = L.s[k];
+        if (i < s.x || i >= s.y) continue;
+        const int hi = (L.t[k] == FFA_CAUSAL) ? min(s.w, i + s.w - s.y + 1) : s.w;
+        if (s.z <= cur && hi > cur) {
+          cur = hi;
+          progressed = true;
+        }
+      }
+    }
+    if (cur < c1) return FFA_TILE_PARTIAL;
+  }
+  return FFA_TILE_FULL;
+}
+
+// Collect, in input order, the valid slices that touch rows [r0,r1) (by_col = false) or
+// columns [c0,c1) (by_col = true) into shared memory (up to kSliceSmem) and into the global
+// per-tile list (up to kSliceCap).  Returns the list to classify with.
+__device__ SliceList gather_slices(const PlanView& v, int n_valid, bool by_col, int lo, int hi, int4* sm_s,
+                                   int* sm_t, int* warp_buf, int* g_nsl, int* g_sl) {
+  int count = 0;
+  for (int c = 0; c < n_valid; c += blockDim.x) {
+    const int r = c + threadIdx.x;
+    int keep = 0;
+    int4 s = make_int4(0, 0, 0, 0);
+    int t = 0;
+    if (r < n_valid) {
+      s = v.slices[r];
+      t = v.stypes[r];
+      if (by_col) {
+        // at the slice's last row every key of [ks, ke) is visible, for both types
+        keep = s.z < hi && s.w > lo;
+      } else {
+        const int a = max(s.x, lo), b = min(s.y, hi);
+        keep = a < b && ((t == FFA_FULL) || (min(s.w, b + s.w - s.y) > s.z));
+      }
+    }
+    int total;
+    const int pos = count + block_exclusive_scan(keep, warp_buf, &total);
+    if (keep) {
+      if (pos < kSliceSmem) {
+        sm_s[pos] = s;
+        sm_t[pos] = t;
+      }
+      if (pos < kSliceCap) g_sl[pos] = r;
+    }
+    count += total;
+  }
+  if (threadIdx.x == 0) *g_nsl = count <= kSliceCap ? count : -1;
+  __syncthreads();
+  SliceList L;
+  if (count <= kSliceSmem) {
+    L.s = sm_s;
+    L.t = sm_t;
+    L.n = count;
+  } else {  // too many to stage: classify against every valid slice
+    L.s = v.slices;
+    L.t = v.stypes;
+    L.n = n_valid;
+  }
+  return L;
+}
+
+// ---------------------------------------------------------------- 2. forward rows
+// One block per forward group.  head_pair: the group is one query tile; otherwise it is the
+// query-tile pair (2g, 2g+1) whose work list is the union of both rows.
+__global__ void __launch_bounds__(256) plan_rows_kernel(ProblemDims P, int head_pair, PlanView v) {
+  __shared__ int4 sm_s[kSliceSmem];
+  __shared__ int sm_t[kSliceSmem];
+  __shared__ uint8_t sm_cls[2][kMaxTiles];
+  __shared__ int warp_buf[32];
+  const int g = blockIdx.x;
+  const int n_valid = v.hdr[0];
+  const int nsub = head_pair ? 1 : 2;
+  for (int sub = 0; sub < nsub; ++sub) {
+    const int qt = head_pair ? g : 2 * g + sub;
+    if (qt >= P.nqt) {
+      for (int kt = threadIdx.x; kt < P.nkt; kt += blockDim.x) sm_cls[sub][kt] = FFA_TILE_EMPTY;
+      __syncthreads();
+      continue;
+    }
+    const int r0 = qt * kTile, r1 = min(r0 + kTile, P.nq);
+    SliceList L = gather_slices(v, n_valid, false, r0, r1, sm_s, sm_t, warp_buf, &v.row_nsl[qt],
+                                &v.row_sl[static_cast<size_t>(qt) * kSliceCap]);
+    for (int kt = threadIdx.x; kt < P.nkt; kt += blockDim.x) {
+      const int c0 = kt * kTile, c1 = min(c0 + kTile, P.nk);
+      const int c = L.n ? classify_tile(L, r0, r1, c0, c1) : FFA_TILE_EMPTY;
+      sm_cls[sub][kt] = static_cast<uint8_t>(c);
+      v.cls[static_cast<size_t>(qt) * P.nkt + kt] = static_cast<uint8_t>(c);
+    }
+    __syncthreads();
+  }
+  // work list: key tiles non-empty for either sub-tile, ascending
+  int count = 0;
+  for (int c = 0; c < P.nkt; c += blockDim.x) {
+    const int kt = c + threadIdx.x;
+    int ca = 0, cb = 0;
+    if (kt < P.nkt) {
+      ca = sm_cls[0][kt];
+      cb = head_pair ? ca : sm_cls[1][kt];
+    }
+    const int keep = (ca | cb) != 0;
+    int total;
+    const int pos = count + block_exclusive_scan(keep, warp_buf, &total);
+    if (keep) v.grp_ent[static_cast<size_t>(g) * P.nkt + pos] = make_entry(kt, ca, cb);
+    count += total;
+  }
+  if (threadIdx.x == 0) v.grp_cnt[g] = count;
+}
+
+// ---------------------------------------------------------------- 2'. backward columns
+// One block per key tile: slices touching the column, class of every tile in the column
+// (same classification function, so the classes equal the row planner's), the list of
+// non-empty query tiles, ascending.
+__global__ void __launch_bounds__(256) plan_cols_kernel(ProblemDims P, PlanView v) {
+  __shared__ int4 sm_s[kSliceSmem];
+  __shared__ int sm_t[kSliceSmem];
+  __shared__ int warp_buf[32];
+  const int kt = blockIdx.x;
+  const int n_valid = v.hdr[0];
+  const int c0 = kt * kTile, c1 = min(c0 + kTile, P.nk);
+  SliceList L = gather_slices(v, n_valid, true, c0, c1, sm_s, sm_t, warp_buf, &v.col_nsl[kt],
+                              &v.col_sl[static_cast<size_t>(kt) * kSliceCap]);
+  int count = 0;
+  for (int c = 0; c < P.nqt; c += blockDim.x) {
+    const int qt = c + threadIdx.x;
+    int cl = 0;
+    if (qt < P.nqt) {
+      const int r0 = qt * kTile, r1 = min(r0 + kTile, P.nq);
+      cl = L.n ? classify_tile(L, r0, r1, c0, c1) : FFA_TILE_EMPTY;
+      v.cls[static_cast<size_t>(qt) * P.nkt + kt] = static_cast<uint8_t>(cl);
+    }
+    const int keep = cl != 0;
+    int total;
+    const int pos = count + block_exclusive_scan(keep, warp_buf, &total);
+    if (keep) v.col_ent[static_cast<size_t>(kt) * P.nqt + pos] = make_entry(qt, cl, cl);
+    count += total;
+  }
+  if (threadIdx.x == 0) v.col_cnt[kt] = count;
+}
+
+// ---------------------------------------------------------------- 3. longest-first order
+// One block: counting sort of `n` lists by length (0..max_len), descending.
+__global__ void __launch_bounds__(1024) plan_order_kernel(const int* __restrict__ cnt, int n, int max_len,
+                                                          int* __restrict__ order) {
+  extern __shared__ int hist[];  // max_len + 1
+  __shared__ int warp_buf[32];
+  for (int i = threadIdx.x; i <= max_len; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[min(max(cnt[i], 0), max_len)], 1);
+  __syncthreads();
+  // start[c] = number of lists longer than c: exclusive scan over c = max_len .. 0
+  const int per = (max_len + 1 + blockDim.x - 1) / blockDim.x;
+  const int lo = threadIdx.x * per;  // position in the reversed array
+  int local = 0;
+  for (int p = lo; p < min(lo + per, max_len + 1); ++p) local += hist[max_len - p];
+  int total;
+  int run = block_exclusive_scan(local, warp_buf, &total);
+  for (int p = lo; p < min(lo + per, max_len + 1); ++p) {
+    const int c = max_len - p;
+    const int h = hist[c];
+    hist[c] = run;
+    run += h;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int pos = atomicAdd(&hist[min(max(cnt[i], 0), max_len)], 1);
+    order[pos] = i;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan_slices(const ProblemDims& P, const int32_t* q_ranges, const int32_t* k_ranges,
+                               const int32_t* types, int R, const PlanView& v, int32_t* status, cudaStream_t s) {
+  plan_slices_kernel<<<1, 1024, 0, s>>>(q_ranges, k_ranges, types, R, P.nq, P.nk, v, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan_rows(const ProblemDims& P, const WsLayout& L, const PlanView& v, cudaStream_t s) {
+  if (L.ngrp == 0) return cudaSuccess;
+  plan_rows_kernel<<<L.ngrp, 256, 0, s>>>(P, L.head_pair ? 1 : 0, v);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = static_cast<size_t>(P.nkt + 1) * sizeof(int);
+  plan_order_kernel<<<1, 1024, smem, s>>>(v.grp_cnt, L.ngrp, P.nkt, v.grp_order);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan_cols(const ProblemDims& P, const PlanView& v, cudaStream_t s) {
+  if (P.nkt == 0) return cudaSuccess;
+  plan_cols_kernel<<<P.nkt, 256, 0, s>>>(P, v);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = static_cast<size_t>(P.nqt + 1) * sizeof(int);
+  plan_order_kernel<<<1, 1024, smem, s>>>(v.col_cnt, P.nkt, P.nqt, v.col_order);
+  return cudaGetLastError();
+}
+
+}  // namespace ffa

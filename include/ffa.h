@@ -1,0 +1,168 @@
+/*
+ * ffa.h -- C ABI of libffa.so: range-masked flash attention for GB300 (sm_103a).
+ *
+ * The operation is the one behind flex_flash_attn_func as described in MagiAttention issue
+ * #180 ("Using dummy/padded attention slices with flex_flash_attn_func for torch.compile
+ * static shapes", question code and maintainer reply): softmax attention over packed tokens
+ * q:[Nq,Hq,d], k,v:[Nk,Hkv,d], masked by a list of slices (q_range, k_range, type), type
+ * 0 = FULL and 1 = CAUSAL, returning out:[Nq,Hq,d] and the per-row log-sum-exp; the
+ * backward pass returns dq, dk, dv.  A slice whose q-range or k-range has start == end
+ * covers no area and is ignored (maintainer reply, "Mechanism").
+ *
+ * Semantics fixed by this library where the pages are silent:
+ *   - CAUSAL is bottom-right aligned inside its slice: pair (i, j) of slice
+ *     [qs,qe) x [ks,ke) is visible iff qs <= i < qe, ks <= j < ke and j <= i + ke - qe.
+ *   - Overlapping slices combine by logical OR (union): a pair is counted once however many
+ *     slices cover it (mask composition by logical operations, Flex Attention paper,
+ *     section 3, "Composability").
+ *   - softcap > 0: score x = softcap * tanh(softmax_scale * q.k / softcap); 0 disables it.
+ *   - softmax_scale <= 0 or NaN selects 1/sqrt(d).
+ *   - Rows with no visible key get out = 0 and lse = -inf; they contribute nothing to any
+ *     gradient and their dq is 0.
+ *   - lse is the natural-log log-sum-exp, float32, laid out [Hq, Nq].
+ *   - GQA: query head h reads key/value head h / (Hq / Hkv).
+ *
+ * Conventions for every entry point:
+ *   - Tensors are contiguous, row-major, bf16 unless stated; pointers marked "device" must
+ *     be device (or managed) memory visible to the current device, 16-byte aligned.
+ *   - The caller owns every buffer, including the workspace; the library keeps no device
+ *     memory between calls.  All work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) without host synchronisation, so outputs are valid only after
+ *     the stream has been synchronised.
+ *   - Errors detectable on the host (null pointers, unsupported shapes, a workspace that is
+ *     too small, misalignment) are returned before anything is launched.  Slice contents
+ *     live on the device: a malformed slice (bound outside [0, N], start > end, unknown
+ *     type) is dropped by the planner, which ORs FFA_STATUS_BAD_RANGE into *status.  A
+ *     bounded wait inside a kernel that runs out ORs FFA_STATUS_TIMEOUT into *status.
+ *     *status is a device int32 that the library only ORs into (the caller clears it);
+ *     it may be NULL.
+ */
+#ifndef FFA_H_
+#define FFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define FFA_OK 0
+#define FFA_ERR_INVALID_ARG 1 /* null pointer, bad shape, n_ranges < 0, misalignment   */
+#define FFA_ERR_UNSUPPORTED 2 /* head_dim not in {64,128}, too many tokens, no sm_103a */
+#define FFA_ERR_CUDA 3        /* a CUDA runtime/driver call failed                     */
+#define FFA_ERR_WORKSPACE 4   /* workspace NULL or smaller than the *_workspace_size() */
+
+/* bits of the device status word */
+#define FFA_STATUS_BAD_RANGE 1 /* a malformed slice was dropped                       */
+#define FFA_STATUS_TIMEOUT 2   /* a bounded wait inside a kernel ran out              */
+
+/* slice types (attn_type_map values) */
+#define FFA_FULL 0
+#define FFA_CAUSAL 1
+
+/* tile classes written by ffa_plan_tiles */
+#define FFA_TILE_EMPTY 0
+#define FFA_TILE_PARTIAL 1
+#define FFA_TILE_FULL 2
+#define FFA_TILE_SIZE 128
+
+/* largest supported total_q / total_k */
+#define FFA_MAX_TOKENS (1 << 20)
+
+typedef struct ffa_shape {
+  int64_t total_q;      /* Nq: packed query tokens, 0 <= Nq <= FFA_MAX_TOKENS           */
+  int64_t total_k;      /* Nk: packed key/value tokens, 0 <= Nk <= FFA_MAX_TOKENS       */
+  int32_t num_heads_q;  /* Hq >= 1                                                      */
+  int32_t num_heads_kv; /* Hkv >= 1, Hq % Hkv == 0                                      */
+  int32_t head_dim;     /* d in {64, 128}                                               */
+} ffa_shape;
+
+/*
+ * Bytes of workspace ffa_fwd / ffa_bwd / ffa_plan_tiles need for this shape and slice count.
+ * The forward workspace holds the planner's output (compacted slices, the tile-class grid,
+ * per-tile-row work lists and their longest-first order); it grows with
+ * ceil(Nq/128) * ceil(Nk/128).  The backward workspace holds the column-wise plan plus the
+ * float32 row statistic D [Hq, Nq] and the float32 dq accumulator [Nq, Hq, d].
+ * Returns 0 for an invalid shape.
+ */
+size_t ffa_fwd_workspace_size(const ffa_shape* shape, int32_t n_ranges);
+size_t ffa_bwd_workspace_size(const ffa_shape* shape, int32_t n_ranges);
+
+/*
+ * Forward pass: out, lse = attention(q, k, v, slices).
+ *   q        device bf16 [Nq, Hq, d]
+ *   k, v     device bf16 [Nk, Hkv, d]
+ *   q_ranges, k_ranges  device int32 [n_ranges, 2] (start, end) pairs, end exclusive
+ *   attn_type_map       device int32 [n_ranges], FFA_FULL or FFA_CAUSAL
+ *   n_ranges            >= 0 (0 means nothing is visible)
+ *   softmax_scale       <= 0 or NaN -> 1/sqrt(d)
+ *   softcap             0 disables; must be >= 0
+ *   out      device bf16 [Nq, Hq, d], written
+ *   lse      device float32 [Hq, Nq], written
+ *   workspace, workspace_bytes  device scratch of at least ffa_fwd_workspace_size() bytes,
+ *            256-byte aligned; contents on entry are ignored
+ *   status   device int32 or NULL (see above)
+ *   stream   cudaStream_t
+ * Results are bit-identical from run to run and under appended start == end slices.
+ */
+int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
+            const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
+            float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+            void* stream);
+
+/*
+ * Backward pass: gradients of sum(out * dout) with respect to q, k and v.
+ *   q, k, v, q_ranges, k_ranges, attn_type_map, n_ranges, softmax_scale, softcap: as for
+ *            ffa_fwd (same values as the forward call)
+ *   out      device bf16 [Nq, Hq, d]: the forward output
+ *   lse      device float32 [Hq, Nq]: the forward log-sum-exp
+ *   dout     device bf16 [Nq, Hq, d]
+ *   dq       device bf16 [Nq, Hq, d], written
+ *   dk, dv   device bf16 [Nk, Hkv, d], written
+ *   workspace  at least ffa_bwd_workspace_size() bytes
+ * dq is accumulated in float32 with atomic adds, so it may differ in the last bits from
+ * run to run; dk and dv are written once per (key tile, kv head).
+ */
+int ffa_bwd(const ffa_shape* shape, const void* q, const void* k, const void* v, const void* out,
+            const float* lse, const void* dout, const int32_t* q_ranges, const int32_t* k_ranges,
+            const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale, float softcap, void* dq,
+            void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * The planner alone: classify every tile of the global 128 x 128 tile grid as
+ * FFA_TILE_EMPTY / PARTIAL / FULL under the union of the slices (block classification of
+ * the Flex Attention paper, section 4, "Block Sparsity" / "Full Block Optimization"),
+ * restricted to in-bounds entries.
+ *   tile_class  device uint8 [ceil(Nq/128), ceil(Nk/128)], written
+ *   by_column   0: the forward planner (one pass per query-tile row);
+ *               1: the backward planner (one pass per key-tile column)
+ *   workspace   at least ffa_fwd_workspace_size() (by_column = 0) or
+ *               ffa_bwd_workspace_size() (by_column = 1) bytes
+ */
+int ffa_plan_tiles(const ffa_shape* shape, const int32_t* q_ranges, const int32_t* k_ranges,
+                   const int32_t* attn_type_map, int32_t n_ranges, int32_t by_column, uint8_t* tile_class,
+                   void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Measurement hook.  When the handles are non-NULL, each later ffa_fwd call records
+ * fwd_start on its stream immediately before the forward attention kernel and fwd_stop
+ * immediately after it (the planner launches stay outside the pair); ffa_bwd does the same
+ * around its main backward kernel with bwd_start / bwd_stop.  The handles are cudaEvent_t
+ * created and owned by the caller; pass NULLs to stop recording.  The setting is
+ * process-wide and not synchronised between threads.  Returns FFA_OK.
+ */
+int ffa_set_kernel_events(void* fwd_start, void* fwd_stop, void* bwd_start, void* bwd_stop);
+
+/* Static description of a return code; never NULL. */
+const char* ffa_status_string(int code);
+
+/* Build description: target architecture, tile sizes, pipeline depths. */
+const char* ffa_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FFA_H_ */

@@ -1,0 +1,79 @@
+"""The C-ABI library builds, loads and exports every symbol include/ffa.h declares; host-side
+argument checks return error codes before anything touches a GPU.  CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import flexible_mask_attention_range_gb300 as ffa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "ffa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ffa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    h = ctypes.CDLL(lib_path)
+    names = _declared_functions()
+    assert "ffa_fwd" in names and "ffa_bwd" in names
+    for n in names:
+        assert hasattr(h, n), f"missing export {n}"
+    assert set(names) <= set(ffa.SIGNATURES), "binding lacks a signature for a declared symbol"
+
+
+def test_build_info_and_status_strings(lib_path):
+    assert "sm_103a" in ffa.ffa_build_info()
+    for code in range(0, 6):
+        assert isinstance(ffa.ffa_status_string(code), str)
+
+
+def test_workspace_sizes(lib_path):
+    a = ffa.ffa_fwd_workspace_size(2048, 2048, 8, 2, 64, 20)
+    b = ffa.ffa_fwd_workspace_size(65536, 65536, 16, 4, 128, 3)
+    c = ffa.ffa_bwd_workspace_size(65536, 65536, 16, 4, 128, 3)
+    assert 0 < a < b < c
+    # the backward workspace holds the fp32 dq accumulator
+    assert c >= 65536 * 16 * 128 * 4
+    assert ffa.ffa_fwd_workspace_size(100, 100, 3, 2, 64, 1) == 0          # Hq % Hkv != 0
+    assert ffa.ffa_fwd_workspace_size(100, 100, 2, 1, 96, 1) == 0          # head_dim
+    assert ffa.ffa_fwd_workspace_size(100, 100, 2, 1, 64, -1) == 0         # n_ranges < 0
+    assert ffa.ffa_fwd_workspace_size((1 << 20) + 1, 8, 2, 1, 64, 1) == 0  # too many tokens
+
+
+def _call_fwd(shape, R=1, softcap=0.0, ptr=16, ws=None, ws_bytes=0):
+    L = ffa.lib()
+    p = ctypes.c_void_p(ptr)
+    return L.ffa_fwd(ctypes.byref(shape) if shape is not None else None, p, p, p, p, p, p, R, -1.0, softcap,
+                     p, p, ws, ws_bytes, None, None)
+
+
+def test_host_argument_checks_return_before_launch(lib_path):
+    s = ffa.FfaShape(256, 256, 2, 1, 64)
+    assert _call_fwd(None) == 1
+    assert _call_fwd(ffa.FfaShape(256, 256, 3, 2, 64)) == 1      # Hq % Hkv
+    assert _call_fwd(ffa.FfaShape(256, 256, 2, 1, 80)) == 2      # unsupported head_dim
+    assert _call_fwd(s, R=-1) == 1
+    assert _call_fwd(s, softcap=-1.0) == 1
+    assert _call_fwd(s, softcap=float("nan")) == 1
+    assert _call_fwd(s, ptr=18) == 1                              # misaligned pointers
+    assert _call_fwd(s, ws=None, ws_bytes=0) == 4                 # no workspace
+    assert _call_fwd(s, ws=ctypes.c_void_p(4096), ws_bytes=16) == 4  # too small
+    assert _call_fwd(ffa.FfaShape(0, 0, 2, 1, 64)) == 0            # empty problem: nothing to do
+    L = ffa.lib()
+    p = ctypes.c_void_p(16)
+    assert L.ffa_bwd(ctypes.byref(ffa.FfaShape(256, 256, 4, 3, 64)), p, p, p, p, p, p, p, p, p, 1, -1.0,
+                     0.0, p, p, p, None, 0, None, None) == 1
+    assert L.ffa_plan_tiles(ctypes.byref(s), None, None, None, 2, 0, p, None, 0, None, None) == 1
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    import flexible_mask_attention_range_gb300.build as b
+    monkeypatch.setattr(b, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(ffa, "_LIB", None)
+    with pytest.raises(ffa.FfaError):
+        ffa.lib()

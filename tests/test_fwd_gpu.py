@@ -1,0 +1,147 @@
+"""Forward parity: the CUDA path against the float64 oracle on identical seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+import flexible_mask_attention_range_gb300 as ffa
+from _parity import assert_lse_close, assert_out_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(lib_path):
+    yield
+
+
+def _inputs(nq, nk, hq, hkv, d, seed):
+    q, k, v, do = W.draw_qkv(nq, nk, hq, hkv, d, seed) if nq == nk else _draw2(nq, nk, hq, hkv, d, seed)
+    return q, k, v, do
+
+
+def _draw2(nq, nk, hq, hkv, d, seed):
+    g = W.make_generator(seed)
+    q = torch.randn(nq, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    do = torch.randn(nq, hq, d, generator=g).to(torch.bfloat16)
+    return q, k, v, do
+
+
+def _run(q, k, v, qr, kr, ty, scale=None, cap=0.0, status=None):
+    out, lse = ffa.ffa_fwd(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, softmax_scale=scale, softcap=cap,
+                           status=status)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _check_full(q, k, v, qr, kr, ty, scale=None, cap=0.0):
+    out, lse = _run(q, k, v, qr, kr, ty, scale, cap)
+    ro, rl = O.forward(q, k, v, qr, kr, ty, softmax_scale=scale, softcap=cap)
+    assert_out_close(to64(out), ro)
+    assert_lse_close(to64(lse), rl)
+    return out, lse
+
+
+@pytest.mark.parametrize("name", ["tiny_256", "page1_2048_gqa"])
+def test_small_workloads_padded_and_unpadded(name):
+    w = W.get(name)
+    q, k, v, _ = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed)
+    o1, l1 = _check_full(q, k, v, w.q_ranges, w.k_ranges, w.types, w.softmax_scale, w.softcap)
+    wp = w.padded()
+    assert len(wp.types) == w.pad_to
+    o2, l2 = _run(q, k, v, wp.q_ranges, wp.k_ranges, wp.types, w.softmax_scale, w.softcap)
+    # padding with start == end slices leaves the forward bit-identical
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_documents_workload_full():
+    w = W.get("docs_16k")
+    q, k, v, _ = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed, with_dout=False)
+    _check_full(q, k, v, w.q_ranges, w.k_ranges, w.types, w.softmax_scale, w.softcap)
+
+
+RANDOM = [
+    # nq, nk, hq, hkv, d, R, cap, seed
+    (1, 1, 1, 1, 64, 1, 0.0, 0),
+    (127, 127, 2, 1, 64, 3, 0.0, 1),
+    (129, 300, 2, 2, 128, 5, 0.0, 2),
+    (300, 129, 4, 2, 64, 7, 5.0, 3),
+    (300, 300, 3, 1, 128, 9, 0.0, 4),
+    (513, 700, 8, 2, 128, 12, 30.0, 5),
+    (700, 513, 6, 3, 64, 20, 0.0, 6),
+    (1000, 1000, 8, 8, 128, 40, 2.0, 7),
+    (1024, 1024, 16, 2, 64, 6, 0.0, 8),
+    (1500, 900, 5, 5, 128, 15, 0.0, 9),
+]
+
+
+@pytest.mark.parametrize("nq,nk,hq,hkv,d,R,cap,seed", RANDOM)
+def test_random_slices(nq, nk, hq, hkv, d, R, cap, seed):
+    q, k, v, _ = _draw2(nq, nk, hq, hkv, d, seed)
+    qr, kr, ty = W.random_slices(nq, nk, R, seed=seed)
+    scale = None if seed % 2 else 0.3
+    _check_full(q, k, v, qr, kr, ty, scale, cap)
+
+
+def test_run_to_run_bit_identical():
+    w = W.get("page1_2048_gqa")
+    q, k, v, _ = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed)
+    a = _run(q, k, v, w.q_ranges, w.k_ranges, w.types)
+    b = _run(q, k, v, w.q_ranges, w.k_ranges, w.types)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_empty_rows_and_no_slices():
+    q, k, v, _ = _draw2(260, 200, 4, 2, 64, 11)
+    # rows [0,50) uncovered, CAUSAL q longer than k: rows 50..149 see nothing
+    qr, kr, ty = [(50, 250), (250, 260)], [(0, 100), (0, 200)], [1, 0]
+    out, lse = _check_full(q, k, v, qr, kr, ty)
+    assert torch.all(out[:150] == 0)
+    assert torch.all(torch.isneginf(lse[:, :150]))
+    out, lse = _run(q, k, v, [(3, 3)], [(0, 200)], [0])
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+    out, lse = _run(q, k, v, torch.zeros(0, 2, dtype=torch.int32), torch.zeros(0, 2, dtype=torch.int32),
+                    torch.zeros(0, dtype=torch.int32))
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_invalid_slice_is_dropped_and_flagged():
+    q, k, v, _ = _draw2(200, 200, 2, 1, 64, 12)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qr, kr, ty = [(0, 200), (10, 5), (0, 10)], [(0, 200), (0, 10), (0, 10)], [1, 0, 9]
+    out, lse = _run(q, k, v, qr, kr, ty, status=st)
+    ro, rl = O.forward(q, k, v, qr[:1], kr[:1], ty[:1])
+    assert_out_close(to64(out), ro)
+    assert_lse_close(to64(lse), rl)
+    assert int(st.item()) == ffa.STATUS_BAD_RANGE
+
+
+def test_flex_flash_attn_func_matches_ffa_fwd():
+    w = W.get("tiny_256")
+    q, k, v, _ = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed)
+    o1, l1 = ffa.flex_flash_attn_func(q.cuda(), k.cuda(), v.cuda(), w.q_ranges, w.k_ranges, w.types,
+                                      max_seqlen_q=w.total, max_seqlen_k=w.total,
+                                      softmax_scale=w.softmax_scale)
+    o2, l2 = _run(q, k, v, w.q_ranges, w.k_ranges, w.types, w.softmax_scale)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["sliding_32k_softcap", "long_causal_64k_prefix"])
+def test_full_size_sampled_rows(name):
+    w = W.get(name)
+    q, k, v, _ = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed, with_dout=False)
+    out, lse = _run(q, k, v, w.q_ranges, w.k_ranges, w.types, w.softmax_scale, w.softcap)
+    g = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 4096, w.total - 1],
+                                     g.integers(0, w.total, 40)]))
+    ro, rl = O.forward(q, k, v, w.q_ranges, w.k_ranges, w.types, softmax_scale=w.softmax_scale,
+                       softcap=w.softcap, rows=rows)
+    assert_out_close(to64(out[rows]), ro)
+    assert_lse_close(to64(lse[:, rows]), rl)
+    # properties at every row: finite outputs, finite LSE (every row sees at least one key)
+    assert torch.isfinite(out.float()).all()
+    assert torch.isfinite(lse).all()
