@@ -25,6 +25,7 @@ CAUSAL = 1
 TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 STATUS_BAD_RANGE = 1
 STATUS_TIMEOUT = 2
+STATUS_SMEM = 4
 TILE = 128
 
 

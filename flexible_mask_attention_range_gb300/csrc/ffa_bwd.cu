@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad + SM::kTotal > SM::kAlloc) {  // cannot place the swizzled tiles: report and stop
-    if (threadIdx.x == 0 && p.status != nullptr) atomicOr(p.status, FFA_STATUS_TIMEOUT);
+    if (threadIdx.x == 0 && p.status != nullptr) atomicOr(p.status, FFA_STATUS_SMEM);
     return;
   }
   uint8_t* sm = smem_raw + pad;

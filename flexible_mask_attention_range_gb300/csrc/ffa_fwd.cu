@@ -371,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int last_use[S];
       for (int s = 0; s < S; ++s) last_use[s] = -1;
+      int last_q = -1;
       for (int wave = 0; ok; ++wave) {
         const int item = sched_item(wave);
         if (item >= p.n_items) break;
@@ -382,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         mbar_arrive_expect_tx(q_full, 2 * SM::kTileBytes);
+        last_q = static_cast<int>(it_cnt);
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) {
           tma_load_2d(sm + SM::kQ0 + b * SM::kBoxBytes, &tmQ, q_full, it.h0 * D + 64 * b, it.qt0 * kTile);
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_abort(abort_flag, p.status);
         // let the copies already issued land before the CTA's shared memory is released
         const uint64_t short_lim = 100000000ull;
-        if (it_cnt > 0 || gk > 0) mbar_wait(q_full, (it_cnt - (gk > 0 && it_cnt == 0 ? 0 : 0)) & 1u, nullptr, 0);
+        if (last_q >= 0) mbar_wait(q_full, static_cast<uint32_t>(last_q) & 1u, nullptr, short_lim);
         for (int s = 0; s < S; ++s) {
           if (last_use[s] < 0) continue;
           mbar_wait(&k_full[s], static_cast<uint32_t>(last_use[s]) & 1u, nullptr, short_lim);
@@ -422,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -489,6 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(drain);
       mbar_wait(drain, 0, nullptr, 100000000ull);
     }
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -57,6 +57,7 @@ extern "C" {
 /* bits of the device status word */
 #define FFA_STATUS_BAD_RANGE 1 /* a malformed slice was dropped                       */
 #define FFA_STATUS_TIMEOUT 2   /* a bounded wait inside a kernel ran out              */
+#define FFA_STATUS_SMEM 4      /* shared memory could not be aligned for the tiles    */
 
 /* slice types (attn_type_map values) */
 #define FFA_FULL 0
