@@ -255,7 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t* ents = p.plan.grp_ent + static_cast<size_t>(it.g) * p.nkt;
       const int nsl = qt < p.nqt ? p.plan.row_nsl[qt] : 0;
       const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
-      float m_run = -INFINITY, l_run = 0.0f;
+      // l_run: sum of the fp32 p (for the LSE); r_run: sum of the bf16-rounded p that the PV
+      // MMA actually multiplies (normalising O by it keeps the weights a convex combination,
+      // so a dominant key is reproduced exactly even when the reference max is stale)
+      float m_run = -INFINITY, l_run = 0.0f, r_run = 0.0f;
       for (int j = 0; j < n; ++j) {
         const uint32_t e = ents[j];
         const int kt = entry_idx(e);
@@ -310,11 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tO + 32 * c, o);
           }
           tmem_wait_st();
-          if (rescale) l_run *= alpha;
+          if (rescale) {
+            l_run *= alpha;
+            r_run *= alpha;
+          }
         }
         if (need) m_run = m_tile;
         const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
-        float sum = 0.0f;
+        float sum = 0.0f, sum_r = 0.0f;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t pk[16];
@@ -325,10 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = kCap ? ex2_approx(x1 + neg_m) : ex2_approx(fmaf(x1, p.scale_log2, neg_m));
             sum += p0 + p1;
             pk[k] = pack_bf16x2(p0, p1);
+            sum_r += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xffff0000u);
           }
           tmem_st16(tS + 16 * c4, pk);
         }
         l_run += sum;
+        r_run += sum_r;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[wg]);
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++o_cnt;
       tc_fence_after();
-      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      const float inv_l = r_run > 0.0f ? 1.0f / r_run : 0.0f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
