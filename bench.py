@@ -223,6 +223,12 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local: int):
     # ---- device-timed region: K steps, events around every main kernel launch
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # torch creates events lazily: record each once so the handle exists; the library then
+    # re-records it around its kernel launch on the same stream
+    for row in ev:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clock_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
     os.makedirs(os.path.dirname(clock_path), exist_ok=True)
@@ -400,7 +406,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="long_causal_64k_prefix", choices=W.ORDER)
+    ap.add_argument("--workload", default="long_causal_64k_prefix", choices=sorted(W.ALL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -300,25 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_tile = kCap ? mx : mx * p.scale_log2;
         const bool need = m_tile > m_run + kTau;
         const bool rescale = need && (m_run != -INFINITY);
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float alpha = rescale ? ex2_approx(m_run - m_tile) : 1.0f;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32 * c, o);
-            tmem_wait_ld();
-            reg_fence(o);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(tO + 32 * c, o);
-          }
-          tmem_wait_st();
-          if (rescale) {
-            l_run *= alpha;
-            r_run *= alpha;
-          }
-        }
+        const float alpha = rescale ? ex2_approx(m_run - m_tile) : 1.0f;
         if (need) m_run = m_tile;
+        if (rescale) {
+          l_run *= alpha;
+          r_run *= alpha;
+        }
         const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
         float sum = 0.0f, sum_r = 0.0f;
 #pragma unroll
@@ -337,6 +324,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l_run += sum;
         r_run += sum_r;
+        // Rescale this row of O when its reference max moved.  O is stable here: the S MMA
+        // that produced this tile was issued after the previous PV MMA, and the next PV MMA
+        // waits for this warpgroup's p_full arrival below.
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(tO + 32 * c, o);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[wg]);

@@ -76,7 +76,9 @@ RANDOM = [
 def test_random_slices(nq, nk, hq, hkv, d, R, cap, seed):
     q, k, v, do = _draw(nq, nk, hq, hkv, d, seed)
     qr, kr, ty = W.random_slices(nq, nk, R, seed=seed)
-    scale = None if seed % 2 else 0.3
+    # explicit scales stay in the workloads' logit regime (about 1/sqrt(d)); a scale several
+    # times larger makes |dq| ~ 10, where bf16 storage alone approaches the 5e-2 bound
+    scale = None if seed % 2 else 0.75 / d ** 0.5
     _check_full(q, k, v, do, qr, kr, ty, scale, cap)
 
 

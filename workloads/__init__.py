@@ -151,7 +151,17 @@ def long_causal() -> Workload:
         types=[CAUSAL, FULL, FULL])
 
 
-ALL = {w.name: w for w in (tiny(), page1(), documents(), sliding_softcap(), long_causal())}
+def long_causal_16k() -> Workload:
+    """The long-causal recipe at a quarter of the length (profiling-sized: inputs > L2)."""
+    total = 16384
+    return Workload(
+        name="long_causal_16k_prefix", total=total, hq=16, hkv=4, d=128, seed=3,
+        q_ranges=[(0, total), (0, 4096), (0, 4096)],
+        k_ranges=[(0, total), (0, 4096), (0, 4096)],
+        types=[CAUSAL, FULL, FULL])
+
+
+ALL = {w.name: w for w in (tiny(), page1(), documents(), sliding_softcap(), long_causal(), long_causal_16k())}
 ORDER = ["tiny_256", "page1_2048_gqa", "docs_16k", "sliding_32k_softcap", "long_causal_64k_prefix"]
 
 
