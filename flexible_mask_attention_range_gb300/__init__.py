@@ -26,6 +26,8 @@ TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 STATUS_BAD_RANGE = 1
 STATUS_TIMEOUT = 2
 STATUS_SMEM = 4
+FWD_NOALLOC_SCRATCH_BYTES = 8 << 20
+ERR_TOO_LARGE = 5
 TILE = 128
 
 
@@ -55,6 +57,8 @@ SIGNATURES = {
                                _P, _P, _P, _P, _SZ, _P, _P]),
     "ffa_plan_tiles": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _I32, _I32, _P, _P, _SZ, _P,
                                       _P]),
+    "ffa_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _I32, _F, _F, _P, _P,
+                                       _P, _P]),
     "ffa_set_kernel_events": (ctypes.c_int, [_P, _P, _P, _P]),
     "ffa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ffa_build_info": (ctypes.c_char_p, []),
@@ -180,6 +184,38 @@ def ffa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_range
                        scale, float(softcap), _ptr(out), _ptr(lse), _ptr(workspace),
                        workspace.numel(), _ptr(status), _stream(dev))
     _check(rc, "ffa_fwd")
+    return out, lse
+
+
+def ffa_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_ranges, attn_type_map,
+                    softmax_scale: Optional[float] = None, softcap: float = 0.0,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    status: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """ffa_fwd without a workspace, for callers that cannot allocate device memory at call
+    time: the library's fixed device scratch array is used instead (see include/ffa.h).
+    Pass preallocated ``out``/``lse`` (and device-resident ranges) to keep the call itself
+    free of allocations."""
+    dev = q.device
+    nq, hq, d = q.shape
+    nk, hkv = k.shape[0], k.shape[1]
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k, "k", torch.bfloat16, dev, (nk, hkv, d))
+    _need(v, "v", torch.bfloat16, dev, (nk, hkv, d))
+    qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
+    if out is None:
+        out = torch.empty(nq, hq, d, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(hq, nq, dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev, (nq, hq, d))
+    _need(lse, "lse", torch.float32, dev, (hq, nq))
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    shp = _shape(nq, nk, hq, hkv, d)
+    scale = -1.0 if softmax_scale is None else float(softmax_scale)
+    rc = lib().ffa_fwd_noalloc(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty),
+                               qr.shape[0], scale, float(softcap), _ptr(out), _ptr(lse), _ptr(status),
+                               _stream(dev))
+    _check(rc, "ffa_fwd_noalloc")
     return out, lse
 
 

@@ -282,6 +282,7 @@ const char* ffa_status_string(int code) {
     case FFA_ERR_UNSUPPORTED: return "unsupported shape or device (needs sm_103a, head_dim 64 or 128)";
     case FFA_ERR_CUDA: return "CUDA call failed";
     case FFA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FFA_ERR_TOO_LARGE: return "problem needs more scratch than the library's fixed device array holds";
     default: return "unknown status";
   }
 }

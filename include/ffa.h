@@ -53,6 +53,7 @@ extern "C" {
 #define FFA_ERR_UNSUPPORTED 2 /* head_dim not in {64,128}, too many tokens, no sm_103a */
 #define FFA_ERR_CUDA 3        /* a CUDA runtime/driver call failed                     */
 #define FFA_ERR_WORKSPACE 4   /* workspace NULL or smaller than the *_workspace_size() */
+#define FFA_ERR_TOO_LARGE 5   /* problem needs more scratch than ffa_fwd_noalloc owns  */
 
 /* bits of the device status word */
 #define FFA_STATUS_BAD_RANGE 1 /* a malformed slice was dropped                       */
@@ -155,6 +156,31 @@ int ffa_plan_tiles(const ffa_shape* shape, const int32_t* q_ranges, const int32_
  * process-wide and not synchronised between threads.  Returns FFA_OK.
  */
 int ffa_set_kernel_events(void* fwd_start, void* fwd_stop, void* bwd_start, void* bwd_stop);
+
+/*
+ * Forward pass for callers that cannot allocate device memory at call time (for example a
+ * runtime that reserves all device memory up front and forbids later cudaMalloc, or a
+ * latency-bound path that cannot afford the device synchronisation an allocation may
+ * cause).  The pages describe no such variant: this entry point has no counterpart there.
+ *
+ * Same arguments and results as ffa_fwd, without the workspace.  The planner's scratch
+ * lives in a fixed device array of FFA_FWD_NOALLOC_SCRATCH_BYTES owned by the library; it
+ * exists once on every device that loads the library and stays allocated until the process
+ * exits.  The function itself allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).  The first call on a device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ *   Returns FFA_ERR_TOO_LARGE (before launching anything) when ffa_fwd_workspace_size()
+ *   for the shape exceeds FFA_FWD_NOALLOC_SCRATCH_BYTES, e.g. beyond about 160K tokens
+ *   with a single query and key range.
+ * Every call uses the same array and the planner overwrites everything it reads, so
+ * nothing has to start at zero; calls whose kernels overlap on the GPU (other streams or
+ * other host threads on the same device) race on the array and must be serialised.
+ */
+#define FFA_FWD_NOALLOC_SCRATCH_BYTES (8u << 20)
+int ffa_fwd_noalloc(const ffa_shape* shape, const void* q, const void* k, const void* v,
+                    const int32_t* q_ranges, const int32_t* k_ranges, const int32_t* attn_type_map,
+                    int32_t n_ranges, float softmax_scale, float softcap, void* out, float* lse,
+                    int32_t* status, void* stream);
 
 /* Static description of a return code; never NULL. */
 const char* ffa_status_string(int code);
