@@ -50,8 +50,8 @@ struct BwdSmem {
   static constexpr int kStat = kDS + kTile * kTile * 2;            // + s * kStatBytes
   static constexpr int kBar = kStat + kStages * kStatBytes;
   // kv_full, kv_empty, qdo_full[S], qdo_empty[S], s_full, dp_full, p_full, ds_full, dq_full,
-  // dq_empty, dkv_full, drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 8;
+  // dq_empty, dkv_full, drain, sds_free
+  static constexpr int kNumBars = 2 + 2 * kStages + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kMaxDyn = 232448;
@@ -193,7 +193,7 @@ template <int D, bool kCap>
 __global__ void __launch_bounds__(kThreads, 1)
     ffa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                   const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using SM = BwdSmem<D>;
   constexpr int S = SM::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_empty = s_full + 5;
   uint64_t* dkv_full = s_full + 6;
   uint64_t* drain = s_full + 7;
+  uint64_t* sds_free = s_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM::kMisc + 4);
 
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_empty, 128);
     mbar_init(dkv_full, 1);
     mbar_init(drain, 1);
+    mbar_init(sds_free, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -341,8 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(p_full);
         // phase 2: dS^T = P' (dP^T - D) -> TMEM (for dK) and shared memory (for dQ)
         ok = __all_sync(0xffffffffu, mbar_wait(dp_full, step_cnt & 1u, abort_flag, lim));
-        if (ok && step_cnt > 0)  // dQ of the previous step has finished reading sDS
-          ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (step_cnt - 1) & 1u, abort_flag, lim));
+        if (ok && step_cnt > 0)  // the previous step's dQ no longer uses sDS (MMA operand, then staging)
+          ok = __all_sync(0xffffffffu, mbar_wait(sds_free, (step_cnt - 1) & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
         const float* Drow = stat + kTile;
@@ -413,9 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) record_abort(abort_flag, p.status);
   } else if (warp < 8) {
     // ------------------------------------------------------------ dQ warpgroup
+    // Reads its dQ row from TMEM (releasing the columns at once), then adds the tile into the
+    // fp32 accumulator with TMA bulk reduce-adds of 32-column boxes staged through the two
+    // 16 KB halves of the dS^T shared tile (free once the dQ MMA has consumed it).
     const int q4 = warp - 4;
     const int r = q4 * 32 + lane;
+    const bool leader = (q4 == 0 && lane == 0);
     const uint32_t tQ = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + 128;
+    uint8_t* sDS = sm + SM::kDS;
     uint32_t step_cnt = 0;
     bool ok = true;
     for (int wave = 0; ok; ++wave) {
@@ -425,30 +432,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < it.n_steps; ++t) {
         const int qt = entry_idx(it.ents[t / p.G]);
         const int h = it.kvh * p.G + (t % p.G);
-        const int i = qt * kTile + r;
-        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, step_cnt & 1u, abort_flag, lim));
+        // one decision for the whole warpgroup: it meets again at named barrier 1 below
+        ok = named_bar_and(1, 128, mbar_wait(dq_full, step_cnt & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
-        float* dst = p.dqacc + (static_cast<size_t>(i) * p.hq + h) * D;
+        uint32_t o[D / 32][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tQ + 32 * c, o);
-          tmem_wait_ld();
-          reg_fence(o);
-          if (i < p.nq) {
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tQ + 32 * c, o[c]);
+        tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              red_add_v4(dst + 32 * c + 4 * k, __uint_as_float(o[4 * k]) * p.scale,
-                         __uint_as_float(o[4 * k + 1]) * p.scale, __uint_as_float(o[4 * k + 2]) * p.scale,
-                         __uint_as_float(o[4 * k + 3]) * p.scale);
-          }
-        }
+        for (int c = 0; c < D / 32; ++c) reg_fence(o[c]);
         tc_fence_before();
         mbar_arrive(dq_empty);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint8_t* buf = sDS + (c & 1) * (kTile * 128);
+          if (c >= 2) {  // the reduce issued from this half two chunks ago has read it
+            if (leader) bulk_wait_group_read<1>();
+            named_bar_sync(1, 128);
+          }
+          uint8_t* rowp = buf + r * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int chunk = k ^ (r & 7);
+            *reinterpret_cast<float4*>(rowp + chunk * 16) =
+                make_float4(__uint_as_float(o[c][4 * k]) * p.scale, __uint_as_float(o[c][4 * k + 1]) * p.scale,
+                            __uint_as_float(o[c][4 * k + 2]) * p.scale, __uint_as_float(o[c][4 * k + 3]) * p.scale);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (leader) {
+            tma_reduce_add_2d(&tmDQ, buf, h * D + 32 * c, qt * kTile);
+            bulk_commit_group();
+          }
+        }
+        if (leader) {
+          bulk_wait_group_read<0>();
+          mbar_arrive(sds_free);
+        }
         ++step_cnt;
       }
     }
+    if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     if (!ok) record_abort(abort_flag, p.status);
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
@@ -647,8 +672,9 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap mq, mk, mv, mdo;
-  if (!encode_tile_map(&mq, a.q, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile) ||
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  if (!encode_tile_map_f32(&mdq, a.dqacc, static_cast<uint64_t>(P.hq) * D, P.nq, 32, kTile) ||
+      !encode_tile_map(&mq, a.q, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile) ||
       !encode_tile_map(&mdo, a.dout, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile) ||
       !encode_tile_map(&mk, a.k, static_cast<uint64_t>(P.hkv) * D, P.nk, 64, kTile) ||
       !encode_tile_map(&mv, a.v, static_cast<uint64_t>(P.hkv) * D, P.nk, 64, kTile))
@@ -674,7 +700,7 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   const int grid = p.n_items < nsm ? p.n_items : nsm;
   if (grid > 0) {
     if (g_kernel_events.bwd_start != nullptr) cudaEventRecord(g_kernel_events.bwd_start, stream);
-    kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, mdo, p);
+    kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, mdo, mdq, p);
     if (g_kernel_events.bwd_stop != nullptr) cudaEventRecord(g_kernel_events.bwd_stop, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -164,6 +164,8 @@ extern KernelEvents g_kernel_events;
 // TMA descriptor creation (ffa_api.cu)
 bool encode_tile_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                      uint32_t box_rows);
+bool encode_tile_map_f32(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                         uint32_t box_rows);
 int num_sms();
 
 }  // namespace ffa
