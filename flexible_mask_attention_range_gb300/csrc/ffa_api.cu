@@ -178,7 +178,8 @@ int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
   a.head_pair = L.head_pair ? 1 : 0;
   a.ngrp = L.ngrp;
   a.slots = L.slots;
-  a.n_items = L.ngrp * L.slots;
+  a.n_items = L.ngrp * L.nch_max * L.slots;
+  a.split = L.split ? 1 : 0;
   a.scale = resolve_scale(softmax_scale, d);
   a.softcap = softcap;
   a.q = q;

@@ -551,14 +551,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.n_steps == 0) continue;
         ok = mbar_wait(kv_full, item_cnt & 1u, abort_flag, lim);
         if (!ok) break;
-        for (int t = 0; t < it.n_steps; ++t) {
+        {  // S^T of the item's first step
           const uint32_t st = gq % S;
           ok = mbar_wait(&qdo_full[st], (gq / S) & 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t q_s = sQ + st * SM::kTileBytes, do_s = sDO + st * SM::kTileBytes;
-          issue_kmajor<D>(tS, sK, q_s, idesc_st);  // S^T = K Q^T
+          issue_kmajor<D>(tS, sK, sQ + st * SM::kTileBytes, idesc_st);  // S^T = K Q^T
           umma_commit(s_full);
+        }
+        for (int t = 0; t < it.n_steps; ++t) {
+          const uint32_t st = gq % S;
+          const uint32_t q_s = sQ + st * SM::kTileBytes, do_s = sDO + st * SM::kTileBytes;
           if (gq > 0) {  // the previous dQ has been drained from the dP^T columns
             ok = mbar_wait(dq_empty, (gq - 1) & 1u, abort_flag, lim);
             if (!ok) break;
@@ -570,6 +573,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_ts<D>(tDV, tS, do_s, idesc_acc, t > 0);  // dV += P^T dO
+          if (t + 1 < it.n_steps) {
+            // S^T of the next step now, so P^T of step t+1 is computed while dK and dQ of this
+            // step run (P^T of step t has been read by the dV MMA issued just before)
+            const uint32_t g1 = gq + 1, st1 = g1 % S;
+            ok = mbar_wait(&qdo_full[st1], (g1 / S) & 1u, abort_flag, lim);
+            if (!ok) break;
+            tc_fence_after();
+            issue_kmajor<D>(tS, sK, sQ + st1 * SM::kTileBytes, idesc_st);
+            umma_commit(s_full);
+          }
           ok = mbar_wait(ds_full, gq & 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();

@@ -62,7 +62,7 @@ struct FwdSmem {
 
 struct FwdParams {
   int nq, nk, hq, hkv, G, nqt, nkt;
-  int head_pair, slots, n_items;
+  int head_pair, slots;
   float scale_log2;  // softmax_scale * log2(e)
   float cap_c;       // softcap * log2(e)
   float cap_k;       // 2 * softmax_scale * log2(e) / softcap
@@ -74,13 +74,22 @@ struct FwdParams {
 };
 
 struct Item {
-  int g, qt0, qt1, h0, h1, kvh;
+  int g, qt0, qt1, h0, h1, kvh, slot;
+  int n;                 // key tiles of this chunk
+  int pslot;             // partial-output slot when the group is split, else -1
+  const uint32_t* ents;  // the chunk's work-list entries
 };
 
+// Work item -> (chunk of a group's work list, head slot).  Chunks are taken longest first.
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int item) {
   Item it;
   const int rank = item / p.slots, slot = item - rank * p.slots;
-  it.g = p.plan.grp_order[rank];
+  const int4 ch = p.plan.chunks[p.plan.chunk_order[rank]];
+  it.g = ch.x;
+  it.n = ch.z - ch.y;
+  it.pslot = ch.w;
+  it.ents = p.plan.grp_ent + static_cast<size_t>(it.g) * p.nkt + ch.y;
+  it.slot = slot;
   if (p.head_pair) {
     it.qt0 = it.qt1 = it.g;
     it.h0 = 2 * slot;
@@ -224,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
+  const int n_items = p.plan.hdr[1] * p.slots;  // chunks x head slots, written by the planner
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
@@ -236,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int wave = 0; ok; ++wave) {
       const int item = sched_item(wave);
-      if (item >= p.n_items) break;
+      if (item >= n_items) break;
       const Item it = decode_item(p, item);
-      const int n = p.plan.grp_cnt[it.g];
+      const int n = it.n;
       const int qt = wg ? it.qt1 : it.qt0;
       const int h = wg ? it.h1 : it.h0;
       const int row = qt * kTile + r;
@@ -252,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const uint32_t* ents = p.plan.grp_ent + static_cast<size_t>(it.g) * p.nkt;
+      const uint32_t* ents = it.ents;
       const int nsl = qt < p.nqt ? p.plan.row_nsl[qt] : 0;
       const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
       // l_run: sum of the fp32 p (for the LSE); r_run: sum of the bf16-rounded p that the PV
@@ -350,27 +360,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++o_cnt;
       tc_fence_after();
       const float inv_l = r_run > 0.0f ? 1.0f / r_run : 0.0f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
+      const float lse_row = l_run > 0.0f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
+      if (it.pslot < 0) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * c, o);
-        tmem_wait_ld();
-        reg_fence(o);
-        if (in_rows) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (in_rows) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-            dst[4 * c + k] = v;
+            for (int k = 0; k < 4; ++k) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+              dst[4 * c + k] = v;
+            }
           }
         }
+        if (in_rows) p.lse[static_cast<size_t>(h) * p.nq + row] = lse_row;
+      } else {
+        // one chunk of a split row: normalised partial O (fp32) and its LSE for the merge
+        const size_t prow = (static_cast<size_t>(it.pslot) * p.slots + it.slot) * 2 * kTile + wg * kTile + r;
+        float4* dst = reinterpret_cast<float4*>(p.plan.part_o + prow * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[8 * c + k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                                         __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+        }
+        p.plan.part_lse[prow] = lse_row;
       }
-      if (in_rows)
-        p.lse[static_cast<size_t>(h) * p.nq + row] = l_run > 0.0f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
     }
     if (!ok) record_abort(abort_flag, p.status);
   } else if (warp == kWarpTma) {
@@ -384,9 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_q = -1;
       for (int wave = 0; ok; ++wave) {
         const int item = sched_item(wave);
-        if (item >= p.n_items) break;
+        if (item >= n_items) break;
         const Item it = decode_item(p, item);
-        const int n = p.plan.grp_cnt[it.g];
+        const int n = it.n;
         if (n == 0) continue;
         if (it_cnt > 0) {
           ok = mbar_wait(q_empty, (it_cnt - 1) & 1u, abort_flag, lim);
@@ -399,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sm + SM::kQ0 + b * SM::kBoxBytes, &tmQ, q_full, it.h0 * D + 64 * b, it.qt0 * kTile);
           tma_load_2d(sm + SM::kQ1 + b * SM::kBoxBytes, &tmQ, q_full, it.h1 * D + 64 * b, it.qt1 * kTile);
         }
-        const uint32_t* ents = p.plan.grp_ent + static_cast<size_t>(it.g) * p.nkt;
+        const uint32_t* ents = it.ents;
         for (int j = 0; j < n; ++j) {
           const int kt = entry_idx(ents[j]);
           const uint32_t st = gk % S, u = gk / S;
@@ -447,9 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int wave = 0; ok; ++wave) {
         const int item = sched_item(wave);
-        if (item >= p.n_items) break;
+        if (item >= n_items) break;
         const Item it = decode_item(p, item);
-        const int n = p.plan.grp_cnt[it.g];
+        const int n = it.n;
         if (n == 0) continue;
         ok = mbar_wait(q_full, it_cnt & 1u, abort_flag, lim);
         if (!ok) break;
@@ -513,6 +541,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// LSE merge of split rows: for a group whose work list was cut into chunks, every row combines
+// its chunks' partial results, L = log sum_c e^{L_c} and O = sum_c e^{L_c - L} O_c (the
+// chunks cover disjoint key sets of the row); rows whose chunks all have L_c = -inf get
+// O = 0 and L = -inf.  One CTA per (group, head slot), one thread per row of either tile.
+template <int D>
+__global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
+  const int g = blockIdx.x / p.slots, slot = blockIdx.x - (blockIdx.x / p.slots) * p.slots;
+  const int nch = p.plan.grp_nch[g];
+  if (nch <= 1) return;
+  const int ps = p.plan.grp_pslot[g];
+  const int sub = threadIdx.x >> 7, r = threadIdx.x & 127;
+  int qt, h;
+  if (p.head_pair) {
+    qt = g;
+    h = 2 * slot + sub;
+  } else {
+    qt = 2 * g + sub;
+    h = slot;
+  }
+  const int row = qt * kTile + r;
+  if (row >= p.nq) return;
+  auto prow = [&](int c) { return (static_cast<size_t>(ps + c) * p.slots + slot) * 2 * kTile + sub * kTile + r; };
+  float mx = -INFINITY;
+  for (int c = 0; c < nch; ++c) mx = fmaxf(mx, p.plan.part_lse[prow(c)]);
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
+  if (mx == -INFINITY) {
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
+    return;
+  }
+  float acc[D];
+#pragma unroll
+  for (int k = 0; k < D; ++k) acc[k] = 0.0f;
+  float wsum = 0.0f;
+  for (int c = 0; c < nch; ++c) {
+    const size_t pr = prow(c);
+    const float w = ex2_approx((p.plan.part_lse[pr] - mx) * kLog2e);
+    wsum += w;
+    const float4* src = reinterpret_cast<const float4*>(p.plan.part_o + pr * D);
+#pragma unroll
+    for (int k = 0; k < D / 4; ++k) {
+      const float4 v = src[k];
+      acc[4 * k] = fmaf(w, v.x, acc[4 * k]);
+      acc[4 * k + 1] = fmaf(w, v.y, acc[4 * k + 1]);
+      acc[4 * k + 2] = fmaf(w, v.z, acc[4 * k + 2]);
+      acc[4 * k + 3] = fmaf(w, v.w, acc[4 * k + 3]);
+    }
+  }
+  const float inv = 1.0f / wsum;
+#pragma unroll
+  for (int k = 0; k < D / 8; ++k) {
+    uint4 v;
+    v.x = pack_bf16x2(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
+    v.y = pack_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
+    v.z = pack_bf16x2(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
+    v.w = pack_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
+    dst[k] = v;
+  }
+  p.lse[static_cast<size_t>(h) * p.nq + row] = mx + lg2_approx(wsum) * kLn2;
+}
+
 template <int D, bool kCap>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   using SM = FwdSmem<D>;
@@ -532,7 +622,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   FwdParams p;
   p.nq = P.nq; p.nk = P.nk; p.hq = P.hq; p.hkv = P.hkv; p.G = P.hq / P.hkv;
   p.nqt = P.nqt; p.nkt = P.nkt;
-  p.head_pair = a.head_pair; p.slots = a.slots; p.n_items = a.n_items;
+  p.head_pair = a.head_pair; p.slots = a.slots;
   p.scale_log2 = a.scale * kLog2e;
   p.cap_c = a.softcap * kLog2e;
   p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
@@ -546,6 +636,9 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   if (g_kernel_events.fwd_start != nullptr) cudaEventRecord(g_kernel_events.fwd_start, stream);
   kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, p);
   if (g_kernel_events.fwd_stop != nullptr) cudaEventRecord(g_kernel_events.fwd_stop, stream);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !a.split) return e;
+  ffa_fwd_merge<D><<<a.ngrp * a.slots, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,12 @@ constexpr int kTile = 128;         // global tile edge (query rows and key colum
 constexpr int kSliceCap = 64;      // slice ids stored per tile row / tile column for masks
 constexpr int kSliceSmem = 512;    // slices staged in shared memory by the planner
 constexpr int kMaxTiles = 8192;    // ceil(FFA_MAX_TOKENS / 128)
+// Forward work lists are cut into chunks when there are too few work items to fill the GPU:
+// the planner then aims at about kSplitTarget chunks (two per SM on a 152-SM part) of at least
+// kMinChunk key tiles, and a merge kernel combines the chunks' partial results by LSE.
+constexpr int kSplitTarget = 304;
+constexpr int kMinChunk = 16;
+constexpr int kMinSplitTiles = 32;
 
 // Entry of a work list: key-tile (or query-tile) index in bits 0..23, class of sub-tile a
 // in bits 24..25 and of sub-tile b in bits 26..27.
@@ -29,8 +35,12 @@ struct WsLayout {
   int nqt = 0, nkt = 0;
   bool head_pair = true;  // forward pairs two query heads of one KV group (else two q-tiles)
   int ngrp = 0, slots = 0;
+  int split_len = 0;      // key tiles per forward chunk (>= nkt: no row is split)
+  int nch_max = 1;        // most chunks one group can have
+  bool split = false;
   size_t hdr = 0, slices = 0, stypes = 0, cls = 0;
-  size_t row_nsl = 0, row_sl = 0, grp_cnt = 0, grp_ent = 0, grp_order = 0;
+  size_t row_nsl = 0, row_sl = 0, grp_cnt = 0, grp_ent = 0;
+  size_t grp_nch = 0, grp_pslot = 0, chunks = 0, chunk_len = 0, chunk_order = 0, part_o = 0, part_lse = 0;
   size_t col_nsl = 0, col_sl = 0, col_cnt = 0, col_ent = 0, col_order = 0;
   size_t rowD = 0, lse2 = 0, dqacc = 0;
   size_t fwd_total = 0, bwd_total = 0;
@@ -47,6 +57,21 @@ inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int 
   L.head_pair = (G % 2 == 0);
   L.ngrp = L.head_pair ? L.nqt : (L.nqt + 1) / 2;
   L.slots = L.head_pair ? hq / 2 : hq;
+  {
+    const int64_t items = static_cast<int64_t>(L.ngrp) * L.slots;
+    L.split_len = L.nkt > 0 ? L.nkt : 1;
+    if (items > 0 && items < kSplitTarget / 2 && L.nkt >= kMinSplitTiles) {
+      const int64_t splits = (kSplitTarget + items - 1) / items;
+      int64_t len = (L.nkt + splits - 1) / splits;
+      if (len < kMinChunk) len = kMinChunk;
+      if (len < L.nkt) {
+        L.split_len = static_cast<int>(len);
+        L.split = true;
+      }
+    }
+    L.nch_max = (L.nkt + L.split_len - 1) / L.split_len;
+    if (L.nch_max < 1) L.nch_max = 1;
+  }
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
   const size_t Rn = static_cast<size_t>(R > 0 ? R : 1);
@@ -61,7 +86,17 @@ inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int 
   L.row_sl = take(nqt * kSliceCap * 4);
   L.grp_cnt = take(ngrp * 4);
   L.grp_ent = take(ngrp * nkt * 4);
-  L.grp_order = take(ngrp * 4);
+  const size_t nch = ngrp * static_cast<size_t>(L.nch_max);
+  L.grp_nch = take(ngrp * 4);
+  L.grp_pslot = take(ngrp * 4);
+  L.chunks = take(nch * 16);
+  L.chunk_len = take(nch * 4);
+  L.chunk_order = take(nch * 4);
+  if (L.split) {  // partial O (fp32) and LSE of every chunk of a split group
+    const size_t rows = nch * static_cast<size_t>(L.slots) * 2 * kTile;
+    L.part_o = take(rows * static_cast<size_t>(d) * 4);
+    L.part_lse = take(rows * 4);
+  }
   L.fwd_total = o;
   o = common;
   L.col_nsl = take(nkt * 4);
@@ -87,7 +122,13 @@ struct PlanView {
   int* row_sl;           // [nqt, kSliceCap]
   int* grp_cnt;          // per forward group: number of work-list entries
   uint32_t* grp_ent;     // [ngrp, nkt]
-  int* grp_order;        // groups, longest list first
+  int* grp_nch;          // chunks of each group
+  int* grp_pslot;        // first partial slot of a split group, -1 if not split
+  int4* chunks;          // (group, first entry, end entry, partial slot or -1); hdr[1] = count
+  int* chunk_len;
+  int* chunk_order;      // chunks, longest first
+  float* part_o;         // [slot][head slot][sub-tile][row][d] partial outputs of split chunks
+  float* part_lse;       // [slot][head slot][sub-tile][row]
   int* col_nsl;          // per key tile: number of slices touching it, -1 if > kSliceCap
   int* col_sl;           // [nkt, kSliceCap]
   int* col_cnt;
@@ -106,7 +147,13 @@ inline PlanView plan_view(const WsLayout& L, void* ws) {
   v.row_sl = reinterpret_cast<int*>(b + L.row_sl);
   v.grp_cnt = reinterpret_cast<int*>(b + L.grp_cnt);
   v.grp_ent = reinterpret_cast<uint32_t*>(b + L.grp_ent);
-  v.grp_order = reinterpret_cast<int*>(b + L.grp_order);
+  v.grp_nch = reinterpret_cast<int*>(b + L.grp_nch);
+  v.grp_pslot = reinterpret_cast<int*>(b + L.grp_pslot);
+  v.chunks = reinterpret_cast<int4*>(b + L.chunks);
+  v.chunk_len = reinterpret_cast<int*>(b + L.chunk_len);
+  v.chunk_order = reinterpret_cast<int*>(b + L.chunk_order);
+  v.part_o = L.split ? reinterpret_cast<float*>(b + L.part_o) : nullptr;
+  v.part_lse = L.split ? reinterpret_cast<float*>(b + L.part_lse) : nullptr;
   v.col_nsl = reinterpret_cast<int*>(b + L.col_nsl);
   v.col_sl = reinterpret_cast<int*>(b + L.col_sl);
   v.col_cnt = reinterpret_cast<int*>(b + L.col_cnt);
@@ -128,7 +175,8 @@ cudaError_t launch_plan_cols(const ProblemDims& P, const PlanView& v, cudaStream
 // Forward (ffa_fwd.cu)
 struct FwdArgs {
   ProblemDims P;
-  int head_pair, ngrp, slots, n_items;
+  int head_pair, ngrp, slots, n_items;  // n_items: upper bound (chunks x slots) for the grid
+  int split;
   float scale, softcap;
   const void *q, *k, *v;
   void* out;

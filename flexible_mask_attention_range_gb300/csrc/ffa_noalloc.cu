@@ -118,7 +118,8 @@ extern "C" int ffa_fwd_noalloc(const ffa_shape* s, const void* q, const void* k,
   a.head_pair = L.head_pair ? 1 : 0;
   a.ngrp = L.ngrp;
   a.slots = L.slots;
-  a.n_items = L.ngrp * L.slots;
+  a.n_items = L.ngrp * L.nch_max * L.slots;
+  a.split = L.split ? 1 : 0;
   a.scale = (!(softmax_scale > 0.0f) || std::isnan(softmax_scale)) ? 1.0f / std::sqrt(static_cast<float>(d))
                                                                      : softmax_scale;
   a.softcap = softcap;

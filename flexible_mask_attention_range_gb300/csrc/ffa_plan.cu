@@ -262,33 +262,75 @@ __global__ void __launch_bounds__(256) plan_cols_kernel(ProblemDims P, PlanView 
 }
 
 // ---------------------------------------------------------------- 3. longest-first order
-// One block: counting sort of `n` lists by length (0..max_len), descending.
-__global__ void __launch_bounds__(1024) plan_order_kernel(const int* __restrict__ cnt, int n, int max_len,
-                                                          int* __restrict__ order) {
-  extern __shared__ int hist[];  // max_len + 1
-  __shared__ int warp_buf[32];
+// Counting sort (one block) of `n` lists by length (0..max_len), descending.  `hist` holds
+// max_len + 1 ints of shared memory.
+__device__ void counting_sort_desc(const int* __restrict__ len, int n, int max_len, int* __restrict__ order,
+                                   int* hist, int* warp_buf) {
   for (int i = threadIdx.x; i <= max_len; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[min(max(cnt[i], 0), max_len)], 1);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[min(max(len[i], 0), max_len)], 1);
   __syncthreads();
   // start[c] = number of lists longer than c: exclusive scan over c = max_len .. 0
   const int per = (max_len + 1 + blockDim.x - 1) / blockDim.x;
   const int lo = threadIdx.x * per;  // position in the reversed array
   int local = 0;
-  for (int p = lo; p < min(lo + per, max_len + 1); ++p) local += hist[max_len - p];
+  for (int q = lo; q < min(lo + per, max_len + 1); ++q) local += hist[max_len - q];
   int total;
   int run = block_exclusive_scan(local, warp_buf, &total);
-  for (int p = lo; p < min(lo + per, max_len + 1); ++p) {
-    const int c = max_len - p;
+  for (int q = lo; q < min(lo + per, max_len + 1); ++q) {
+    const int c = max_len - q;
     const int h = hist[c];
     hist[c] = run;
     run += h;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int pos = atomicAdd(&hist[min(max(cnt[i], 0), max_len)], 1);
+    const int pos = atomicAdd(&hist[min(max(len[i], 0), max_len)], 1);
     order[pos] = i;
   }
+}
+
+__global__ void __launch_bounds__(1024) plan_order_kernel(const int* __restrict__ cnt, int n, int max_len,
+                                                          int* __restrict__ order) {
+  extern __shared__ int hist[];
+  __shared__ int warp_buf[32];
+  counting_sort_desc(cnt, n, max_len, order, hist, warp_buf);
+}
+
+// ---------------------------------------------------------------- 3'. forward chunks
+// One block.  Cuts every group's work list into chunks of at most `split_len` entries (one
+// chunk, possibly empty, when the list is short), gives the chunks of split groups
+// consecutive partial-output slots, and orders all chunks longest first.  hdr[1] = chunks.
+__global__ void __launch_bounds__(1024) plan_chunks_kernel(int ngrp, int split_len, PlanView v) {
+  extern __shared__ int hist[];  // split_len + 1
+  __shared__ int warp_buf[32];
+  int base = 0, pbase = 0;
+  for (int c = 0; c < ngrp; c += blockDim.x) {
+    const int g = c + threadIdx.x;
+    int cnt = 0, nch = 0;
+    if (g < ngrp) {
+      cnt = v.grp_cnt[g];
+      nch = max(1, (cnt + split_len - 1) / split_len);
+    }
+    const bool split = nch > 1;
+    int total, ptotal;
+    const int pos = base + block_exclusive_scan(nch, warp_buf, &total);
+    const int ppos = pbase + block_exclusive_scan(split ? nch : 0, warp_buf, &ptotal);
+    if (g < ngrp) {
+      v.grp_nch[g] = nch;
+      v.grp_pslot[g] = split ? ppos : -1;
+      for (int k = 0; k < nch; ++k) {
+        const int e0 = k * split_len, e1 = min(cnt, e0 + split_len);
+        v.chunks[pos + k] = make_int4(g, e0, e1, split ? ppos + k : -1);
+        v.chunk_len[pos + k] = e1 - e0;
+      }
+    }
+    base += total;
+    pbase += ptotal;
+  }
+  if (threadIdx.x == 0) v.hdr[1] = base;
+  __syncthreads();
+  counting_sort_desc(v.chunk_len, base, split_len, v.chunk_order, hist, warp_buf);
 }
 
 }  // namespace
@@ -304,8 +346,8 @@ cudaError_t launch_plan_rows(const ProblemDims& P, const WsLayout& L, const Plan
   plan_rows_kernel<<<L.ngrp, 256, 0, s>>>(P, L.head_pair ? 1 : 0, v);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = static_cast<size_t>(P.nkt + 1) * sizeof(int);
-  plan_order_kernel<<<1, 1024, smem, s>>>(v.grp_cnt, L.ngrp, P.nkt, v.grp_order);
+  const size_t smem = static_cast<size_t>(L.split_len + 1) * sizeof(int);
+  plan_chunks_kernel<<<1, 1024, smem, s>>>(L.ngrp, L.split_len, v);
   return cudaGetLastError();
 }
 

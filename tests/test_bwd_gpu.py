@@ -69,6 +69,7 @@ RANDOM = [
     (513, 700, 8, 2, 128, 12, 30.0, 5),
     (700, 513, 6, 3, 64, 20, 0.0, 6),
     (1000, 1000, 8, 8, 128, 40, 2.0, 7),
+    (64, 9000, 2, 1, 128, 4, 0.0, 8),      # forward rows split across CTAs
 ]
 
 

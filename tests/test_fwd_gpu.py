@@ -131,6 +131,29 @@ def test_flex_flash_attn_func_matches_ffa_fwd():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+# Few work items and long key ranges: the planner cuts each row's work list into chunks that
+# run on different SMs, and the LSE merge combines them.
+SPLIT = [
+    # nq, nk, hq, hkv, d, cap, seed, slices
+    (64, 16384, 2, 1, 128, 0.0, 31, ([(0, 64), (0, 32)], [(0, 16384), (0, 100)], [1, 0])),
+    (300, 9000, 3, 1, 64, 0.0, 32, None),
+    (129, 20000, 8, 8, 128, 5.0, 33, ([(0, 129), (100, 129), (0, 10)], [(0, 20000), (5000, 5200), (7, 7)],
+                                       [1, 0, 0])),
+    (1, 40000, 2, 2, 64, 0.0, 34, ([(0, 1)], [(0, 40000)], [1])),
+]
+
+
+@pytest.mark.parametrize("nq,nk,hq,hkv,d,cap,seed,sl", SPLIT)
+def test_split_rows_lse_merge(nq, nk, hq, hkv, d, cap, seed, sl):
+    q, k, v, _ = _draw2(nq, nk, hq, hkv, d, seed)
+    qr, kr, ty = sl if sl is not None else W.random_slices(nq, nk, 14, seed=seed)
+    out, lse = _check_full(q, k, v, qr, kr, ty, None, cap)
+    again = _run(q, k, v, qr, kr, ty, None, cap)
+    assert torch.equal(out, again[0]) and torch.equal(lse, again[1])
+    pad = _run(q, k, v, list(qr) + [(0, 0), (3, 3)], list(kr) + [(0, 0), (0, nk)], list(ty) + [0, 1], None, cap)
+    assert torch.equal(out, pad[0]) and torch.equal(lse, pad[1])
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["sliding_32k_softcap", "long_causal_64k_prefix"])
 def test_full_size_sampled_rows(name):
