@@ -83,6 +83,13 @@ def test_random_slices(nq, nk, hq, hkv, d, R, cap, seed):
     _check_full(q, k, v, do, qr, kr, ty, scale, cap)
 
 
+@pytest.mark.parametrize("scale,cap", [(1.0, 1.0), (0.05, 50.0), (0.2, 3.0)])
+def test_softcap_polynomial_and_exact_paths(scale, cap):
+    q, k, v, do = _draw(400, 700, 4, 2, 128, 41)
+    qr, kr, ty = [(0, 400), (100, 300)], [(0, 700), (0, 150)], [1, 0]
+    _check_full(q, k, v, do, qr, kr, ty, scale, cap)
+
+
 def test_empty_rows_and_unseen_keys_have_zero_gradients():
     q, k, v, do = _draw(260, 300, 4, 2, 64, 11)
     qr, kr, ty = [(50, 250), (250, 260)], [(0, 100), (0, 200)], [1, 0]   # keys >= 200 unseen

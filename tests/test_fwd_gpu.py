@@ -88,6 +88,15 @@ def test_random_slices(nq, nk, hq, hkv, d, R, cap, seed):
     _check_full(q, k, v, qr, kr, ty, scale, cap)
 
 
+@pytest.mark.parametrize("scale,cap", [(1.0, 1.0), (0.05, 50.0), (0.2, 3.0)])
+def test_softcap_polynomial_and_exact_paths(scale, cap):
+    """Large logits (|scale*q.k/softcap| beyond the tanh polynomial's range) take the exact
+    form, small ones the polynomial; some warps mix both across tiles."""
+    q, k, v, _ = _draw2(400, 700, 4, 2, 128, 41)
+    qr, kr, ty = [(0, 400), (100, 300)], [(0, 700), (0, 150)], [1, 0]
+    _check_full(q, k, v, qr, kr, ty, scale, cap)
+
+
 def test_run_to_run_bit_identical():
     w = W.get("page1_2048_gqa")
     q, k, v, _ = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed)
