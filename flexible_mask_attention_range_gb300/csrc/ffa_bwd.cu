@@ -17,11 +17,14 @@
 //      dK and dV stay in TMEM for the whole item and are written once.
 //   3. ffa_bwd_dq_convert: fp32 accumulator -> bf16 dq.
 //
-// Warp roles (320 threads):
-//   warps 0-3  compute warpgroup: key row r of the tile <-> TMEM lane r; P^T, dS^T, epilogue
-//   warps 4-7  dQ warpgroup: query row r <-> TMEM lane r; drains dQ into the accumulator
-//   warp 8     TMA producer;  warp 9  MMA issuer (owns TMEM)
-// TMEM columns: S^T/P^T [0,128), dP^T/dS^T then dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
+// Warp roles (448 threads):
+//   warps 0-7  two compute warpgroups: warpgroup h handles query columns [64h, 64h+64) of the
+//              tile, key row r <-> TMEM lane r; P^T, dS^T; epilogue (h = 0: dV, h = 1: dK)
+//   warps 8-11 dQ warpgroup: query row r <-> TMEM lane r; drains dQ into the accumulator
+//   warp 12    TMA producer;  warp 13  MMA issuer (owns TMEM)
+// TMEM columns: S^T [0,128) with P^T of half h (bf16) over [64h, 64h+32); dP^T [128,256) with
+// dS^T of half h over [128+64h, 128+64h+32), then dQ [128,128+D); dV [256,256+D),
+// dK [256+D,256+2D).
 #include <algorithm>
 
 #include "ffa_internal.h"
@@ -32,9 +35,10 @@ namespace ffa {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 320;
-constexpr int kWarpTma = 8;
-constexpr int kWarpMma = 9;
+constexpr int kThreads = 448;
+constexpr int kWarpDq = 8;
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;
 
 template <int D>
 struct BwdSmem {
@@ -154,14 +158,16 @@ __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t sA, uint3
   }
 }
 
-// D (+)= A[tmem] x B where B is a 128-row (K) tile of N columns stored MN-major
+// D (+)= A[tmem] x B where B is a 128-row (K) tile of N columns stored MN-major.  A (bf16,
+// K = 128 queries) sits in two halves: queries [0,64) at columns [0,32) of a_tmem and
+// queries [64,128) at columns [64,96).
 template <int N>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc,
                                         bool accumulate) {
 #pragma unroll
   for (int s = 0; s < kTile / 16; ++s)
-    umma_ts(d_tmem, a_tmem + s * 8, make_sdesc(sB + s * 2048, kTile * 128, 1024, kSwizzle128B), idesc,
-            (accumulate || s > 0) ? 1u : 0u);
+    umma_ts(d_tmem, a_tmem + (s / 4) * 64 + (s % 4) * 8, make_sdesc(sB + s * 2048, kTile * 128, 1024, kSwizzle128B),
+            idesc, (accumulate || s > 0) ? 1u : 0u);
 }
 
 // dQ = dS K: A = dS^T stored [key][query] (MN-major, 2 boxes of 64 queries), B = K tile [key][d]
@@ -230,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(p_full, 256);
+    mbar_init(ds_full, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(dkv_full, 1);
@@ -256,13 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
 
-  if (warp < 4) {
-    // ------------------------------------------------------------ compute warpgroup
-    const int r = warp * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tbase + lane_base, tP = tbase + lane_base + 128;
-    const uint32_t tDV = tbase + lane_base + 256, tDK = tbase + lane_base + 256 + D;
-    uint8_t* sDS = sm + SM::kDS;
+  if (warp < 8) {
+    // ------------------------------------------------------------ compute warpgroups
+    const int hf = warp >> 2, q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int c0 = hf * 64;  // first query column of this warpgroup
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tbase + lane_base + c0, tP = tbase + lane_base + 128 + c0;
+    const uint32_t tOut = tbase + lane_base + 256 + hf * D;  // hf 0: dV, hf 1: dK
+    uint8_t* sDS = sm + SM::kDS + hf * (kTile * 128);
     uint32_t step_cnt = 0, item_cnt = 0;
     bool ok = true;
     for (int wave = 0; ok; ++wave) {
@@ -272,15 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = it.kt * kTile + r;  // key row
       const bool in_keys = j < p.nk;
       const size_t orow = (static_cast<size_t>(j) * p.hkv + it.kvh) * D;
+      __nv_bfloat16* gout = hf ? p.dk : p.dv;
       if (it.n_steps == 0) {
         if (in_keys) {
-          uint4* a = reinterpret_cast<uint4*>(p.dk + orow);
-          uint4* b = reinterpret_cast<uint4*>(p.dv + orow);
+          uint4* a = reinterpret_cast<uint4*>(gout + orow);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            a[c] = make_uint4(0u, 0u, 0u, 0u);
-            b[c] = make_uint4(0u, 0u, 0u, 0u);
-          }
+          for (int c = 0; c < D / 8; ++c) a[c] = make_uint4(0u, 0u, 0u, 0u);
         }
         continue;
       }
@@ -300,41 +305,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[4];
         const bool masked = (cls != FFA_TILE_FULL) || (qt * kTile + kTile > p.nq) || !in_keys;
         if (masked) key_mask(p, cls, j, qt, nsl, sl, w);
-        // phase 1: P^T from S^T and the row LSEs; keep P' = P (or P (1 - tanh^2)) as bf16
-        uint32_t pp[64];
+        // phase 1: P^T of this warpgroup's 64 queries from S^T and the row LSEs; keep
+        // P' = P (or P (1 - tanh^2) with softcap) packed as bf16 for phase 2
+        uint32_t pp[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t sv[32];
           tmem_ld32(tS + 32 * c, sv);
           tmem_wait_ld();
           reg_fence(sv);
           uint32_t pk[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float pv[2], pd[2];
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(stat + c0 + 32 * c + 4 * k4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float pv[4], pd[4];
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int col = 32 * c + 2 * k + h2;
-              const float s = __uint_as_float(sv[2 * k + h2]);
-              const float l2 = stat[col];
+            for (int h4 = 0; h4 < 4; ++h4) {
+              const int col = c0 + 32 * c + 4 * k4 + h4;
+              const float s = __uint_as_float(sv[4 * k4 + h4]);
               float pr;
               if (kCap) {
                 const float x = capped_log2(s, p.cap_c, p.cap_k);
-                pr = ex2_approx(x - l2);
+                pr = ex2_approx(x - lv[h4]);
                 const float th = x * p.inv_cap_c;
-                pd[h2] = pr * (1.0f - th * th);
+                pd[h4] = pr * (1.0f - th * th);
               } else {
-                pr = ex2_approx(fmaf(s, p.scale_log2, -l2));
-                pd[h2] = pr;
+                pr = ex2_approx(fmaf(s, p.scale_log2, -lv[h4]));
+                pd[h4] = pr;
               }
               if (masked && !((w[col >> 5] >> (col & 31)) & 1u)) {
                 pr = 0.0f;
-                pd[h2] = 0.0f;
+                pd[h4] = 0.0f;
               }
-              pv[h2] = pr;
+              pv[h4] = pr;
             }
-            pk[k] = pack_bf16x2(pv[0], pv[1]);
-            pp[16 * c + k] = pack_bf16x2(pd[0], pd[1]);
+            pk[2 * k4] = pack_bf16x2(pv[0], pv[1]);
+            pk[2 * k4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            if (kCap) {
+              pp[16 * c + 2 * k4] = pack_bf16x2(pd[0], pd[1]);
+              pp[16 * c + 2 * k4 + 1] = pack_bf16x2(pd[2], pd[3]);
+            } else {
+              pp[16 * c + 2 * k4] = pk[2 * k4];
+              pp[16 * c + 2 * k4 + 1] = pk[2 * k4 + 1];
+            }
           }
           tmem_st16(tS + 16 * c, pk);
         }
@@ -349,28 +363,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float* Drow = stat + kTile;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t dv[32];
           tmem_ld32(tP + 32 * c, dv);
           tmem_wait_ld();
           reg_fence(dv);
           uint32_t pk[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const uint32_t pr = pp[16 * c + k];
-            const float p0 = __uint_as_float(pr << 16), p1 = __uint_as_float(pr & 0xffff0000u);
-            const int col = 32 * c + 2 * k;
-            const float d0 = p0 * (__uint_as_float(dv[2 * k]) - Drow[col]);
-            const float d1 = p1 * (__uint_as_float(dv[2 * k + 1]) - Drow[col + 1]);
-            pk[k] = pack_bf16x2(d0, d1);
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(Drow + c0 + 32 * c + 4 * k4);
+            const uint32_t pa = pp[16 * c + 2 * k4], pb = pp[16 * c + 2 * k4 + 1];
+            const float d0 = __uint_as_float(pa << 16) * (__uint_as_float(dv[4 * k4]) - d4.x);
+            const float d1 = __uint_as_float(pa & 0xffff0000u) * (__uint_as_float(dv[4 * k4 + 1]) - d4.y);
+            const float d2 = __uint_as_float(pb << 16) * (__uint_as_float(dv[4 * k4 + 2]) - d4.z);
+            const float d3 = __uint_as_float(pb & 0xffff0000u) * (__uint_as_float(dv[4 * k4 + 3]) - d4.w);
+            pk[2 * k4] = pack_bf16x2(d0, d1);
+            pk[2 * k4 + 1] = pack_bf16x2(d2, d3);
           }
           tmem_st16(tP + 16 * c, pk);
-          // shared-memory copy: row r, queries 32c..32c+31 -> half c/2, 16-byte chunks
-          // (c%2)*4 .. +3, 128-byte swizzle (chunk ^= row % 8)
-          uint8_t* rowp = sDS + (c >> 1) * (kTile * 128) + r * 128;
+          // shared-memory copy: row r, this half's queries 32c..32c+31 -> 16-byte chunks
+          // c*4 .. c*4+3 of the half's 128-byte row, 128-byte swizzle (chunk ^= row % 8)
+          uint8_t* rowp = sDS + r * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int chunk = ((c & 1) * 4 + q) ^ (r & 7);
+            const int chunk = (c * 4 + q) ^ (r & 7);
             *reinterpret_cast<uint4*>(rowp + chunk * 16) =
                 make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           }
@@ -382,43 +398,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++step_cnt;
       }
       if (!ok) break;
-      // epilogue: dV and scale * dK of this key tile
+      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK of this key tile
       ok = __all_sync(0xffffffffu, mbar_wait(dkv_full, item_cnt & 1u, abort_flag, lim));
       if (!ok) break;
       ++item_cnt;
       tc_fence_after();
+      const float f = hf ? p.scale : 1.0f;
+      uint4* dst = reinterpret_cast<uint4*>(gout + orow);
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t tsrc = which ? tDK : tDV;
-        const float f = which ? p.scale : 1.0f;
-        uint4* dst = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + orow);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tOut + 32 * c, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        if (in_keys) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tsrc + 32 * c, o);
-          tmem_wait_ld();
-          reg_fence(o);
-          if (in_keys) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * f, __uint_as_float(o[8 * k + 1]) * f);
-              v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * f, __uint_as_float(o[8 * k + 3]) * f);
-              v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * f, __uint_as_float(o[8 * k + 5]) * f);
-              v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * f, __uint_as_float(o[8 * k + 7]) * f);
-              dst[4 * c + k] = v;
-            }
+          for (int k = 0; k < 4; ++k) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * f, __uint_as_float(o[8 * k + 1]) * f);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * f, __uint_as_float(o[8 * k + 3]) * f);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * f, __uint_as_float(o[8 * k + 5]) * f);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * f, __uint_as_float(o[8 * k + 7]) * f);
+            dst[4 * c + k] = v;
           }
         }
       }
     }
     if (!ok) record_abort(abort_flag, p.status);
-  } else if (warp < 8) {
+  } else if (warp < kWarpTma) {
     // ------------------------------------------------------------ dQ warpgroup
-    // Reads its dQ row from TMEM (releasing the columns at once), then adds the tile into the
-    // fp32 accumulator with TMA bulk reduce-adds of 32-column boxes staged through the two
-    // 16 KB halves of the dS^T shared tile (free once the dQ MMA has consumed it).
-    const int q4 = warp - 4;
+    // Reads its dQ row from TMEM (64 columns at a time; the columns are released once the
+    // whole row is in registers), then adds the tile into the fp32 accumulator with TMA bulk
+    // reduce-adds of 32-column boxes staged through the two 16 KB halves of the dS^T shared
+    // tile (free once the dQ MMA has consumed it).
+    const int q4 = warp - kWarpDq;
     const int r = q4 * 32 + lane;
     const bool leader = (q4 == 0 && lane == 0);
     const uint32_t tQ = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + 128;
@@ -436,34 +449,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = named_bar_and(1, 128, mbar_wait(dq_full, step_cnt & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
-        uint32_t o[D / 32][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(tQ + 32 * c, o[c]);
-        tmem_wait_ld();
+        for (int half = 0; half < D / 64; ++half) {
+          uint32_t o[2][32];
+          tmem_ld32(tQ + 64 * half, o[0]);
+          tmem_ld32(tQ + 64 * half + 32, o[1]);
+          tmem_wait_ld();
+          reg_fence(o[0]);
+          reg_fence(o[1]);
+          if (half == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+          }
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) reg_fence(o[c]);
-        tc_fence_before();
-        mbar_arrive(dq_empty);
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * half + cc;
+            uint8_t* buf = sDS + (c & 1) * (kTile * 128);
+            if (c >= 2) {  // the reduce issued from this half two chunks ago has read it
+              if (leader) bulk_wait_group_read<1>();
+              named_bar_sync(1, 128);
+            }
+            uint8_t* rowp = buf + r * 128;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint8_t* buf = sDS + (c & 1) * (kTile * 128);
-          if (c >= 2) {  // the reduce issued from this half two chunks ago has read it
-            if (leader) bulk_wait_group_read<1>();
+            for (int k = 0; k < 8; ++k) {
+              const int chunk = k ^ (r & 7);
+              *reinterpret_cast<float4*>(rowp + chunk * 16) = make_float4(
+                  __uint_as_float(o[cc][4 * k]) * p.scale, __uint_as_float(o[cc][4 * k + 1]) * p.scale,
+                  __uint_as_float(o[cc][4 * k + 2]) * p.scale, __uint_as_float(o[cc][4 * k + 3]) * p.scale);
+            }
+            fence_proxy_async_smem();
             named_bar_sync(1, 128);
-          }
-          uint8_t* rowp = buf + r * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int chunk = k ^ (r & 7);
-            *reinterpret_cast<float4*>(rowp + chunk * 16) =
-                make_float4(__uint_as_float(o[c][4 * k]) * p.scale, __uint_as_float(o[c][4 * k + 1]) * p.scale,
-                            __uint_as_float(o[c][4 * k + 2]) * p.scale, __uint_as_float(o[c][4 * k + 3]) * p.scale);
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (leader) {
-            tma_reduce_add_2d(&tmDQ, buf, h * D + 32 * c, qt * kTile);
-            bulk_commit_group();
+            if (leader) {
+              tma_reduce_add_2d(&tmDQ, buf, h * D + 32 * c, qt * kTile);
+              bulk_commit_group();
+            }
           }
         }
         if (leader) {
