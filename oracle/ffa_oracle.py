@@ -22,6 +22,11 @@ each row's whole key set):
     reading taken here: x = softcap * tanh(scale * q.k / softcap), softcap = 0 disables it.
   * Safe softmax (same paper, section 1): rows with no visible key produce O = 0 and
     LSE = -inf instead of NaN.
+  * ALiBi score modification (same paper, sections 2 and 3.1: ALiBi adds a distance-based,
+    position-dependent bias to the score): optional per-query-head slopes; reading taken
+    here: x_ij = softcap(scale * q.k) + slope_h * (j - i) with i, j the packed token
+    positions (the distance between two tokens of one document equals their in-document
+    distance).
 
 Readings where the pages are silent (each is listed in the design notes):
   * CAUSAL alignment inside a slice with unequal q and k lengths: bottom-right.  Pair (i, j)
@@ -231,10 +236,11 @@ def _capped(s: np.ndarray, softcap: float) -> np.ndarray:
     return s
 
 
-def _row_block_stats(qb, kk, m, scale, softcap):
+def _row_block_stats(qb, kk, m, scale, softcap, bias=None):
     """For one head and one row block: S, X, LSE and P per the definition."""
     s = scale * (qb @ kk.T)
-    x = np.where(m, _capped(s, softcap), -np.inf)
+    xb = _capped(s, softcap) if bias is None else _capped(s, softcap) + bias
+    x = np.where(m, xb, -np.inf)
     has = m.any(axis=1)
     mx = np.where(has, np.max(np.where(m, x, -np.inf), axis=1, initial=-np.inf), 0.0)
     with np.errstate(under="ignore"):
@@ -252,8 +258,15 @@ def _span(lo: np.ndarray, hi: np.ndarray) -> Tuple[int, int]:
     return int(lo[ne].min()), int(hi[ne].max())
 
 
+def _alibi(slopes, h, rows, c0, c1):
+    if slopes is None:
+        return None
+    return float(slopes[h]) * (np.arange(c0, c1, dtype=np.float64)[None, :] - np.asarray(rows, dtype=np.float64)[:, None])
+
+
 def forward(q, k, v, q_ranges, k_ranges, attn_type_map, softmax_scale=None,
-            softcap: float = 0.0, rows: Optional[Sequence[int]] = None, block: int = 128):
+            softcap: float = 0.0, rows: Optional[Sequence[int]] = None, block: int = 128,
+            alibi_slopes: Optional[Sequence[float]] = None):
     """O and LSE.  Returns (out [n, Hq, d] f64, lse [Hq, n] f64) for all rows or ``rows``."""
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     nq, hq, d = q.shape
@@ -275,15 +288,17 @@ def forward(q, k, v, q_ranges, k_ranges, attn_type_map, softmax_scale=None,
         m = mask_block(rel, rb, c0, c1)
         for h in range(hq):
             kh = h // g
-            _, p, l = _row_block_stats(q[rb, h], k[c0:c1, kh], m, scale, softcap)
+            _, p, l = _row_block_stats(q[rb, h], k[c0:c1, kh], m, scale, softcap,
+                                       _alibi(alibi_slopes, h, rb, c0, c1))
             out[b0:b0 + len(rb), h] = p @ v[c0:c1, kh]
             lse[h, b0:b0 + len(rb)] = l
     return out, lse
 
 
-def _grad_block(qb, kk, vv, dob, m, scale, softcap):
-    """Analytic gradients of sum(O * dO) for one head and one row block."""
-    s, p, _ = _row_block_stats(qb, kk, m, scale, softcap)
+def _grad_block(qb, kk, vv, dob, m, scale, softcap, bias=None):
+    """Analytic gradients of sum(O * dO) for one head and one row block (the ALiBi bias
+    does not depend on q or k, so it enters through P only)."""
+    s, p, _ = _row_block_stats(qb, kk, m, scale, softcap, bias)
     dp = dob @ vv.T
     dd = np.sum(p * dp, axis=1, keepdims=True)        # D_i = sum_j P_ij dP_ij
     dx = p * (dp - dd)
@@ -300,7 +315,8 @@ def _grad_block(qb, kk, vv, dob, m, scale, softcap):
 
 def backward(q, k, v, dout, q_ranges, k_ranges, attn_type_map, softmax_scale=None,
              softcap: float = 0.0, rows: Optional[Sequence[int]] = None,
-             keys: Optional[Sequence[int]] = None, block: int = 128):
+             keys: Optional[Sequence[int]] = None, block: int = 128,
+             alibi_slopes: Optional[Sequence[float]] = None):
     """Gradients of sum(O * dO) w.r.t. q, k, v (analytic, float64).
 
     With neither ``rows`` nor ``keys``: full (dq [Nq,Hq,d], dk, dv [Nk,Hkv,d]).
@@ -354,7 +370,7 @@ def backward(q, k, v, dout, q_ranges, k_ranges, attn_type_map, softmax_scale=Non
         for h in range(hq):
             kh = h // g
             gq, gk, gv = _grad_block(q[rb, h], k[c0:c1, kh], v[c0:c1, kh], do[rb, h], m,
-                                     scale, softcap)
+                                     scale, softcap, _alibi(alibi_slopes, h, rb, c0, c1))
             if want_dq:
                 dq[b0:b0 + len(rb), h] = gq
             if want_dkv:

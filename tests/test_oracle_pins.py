@@ -352,8 +352,8 @@ def test_planted_dropped_gradient_term_is_caught(monkeypatch):
     import oracle.ffa_oracle as M
     orig = M._grad_block
 
-    def wrong(qb, kk, vv, dob, m, scale, softcap):
-        dq, dk, dv = orig(qb, kk, vv, dob, m, scale, softcap)
+    def wrong(*args, **kwargs):
+        dq, dk, dv = orig(*args, **kwargs)
         return dq, dk, dv * 0.999
     monkeypatch.setattr(M, "_grad_block", wrong)
     with pytest.raises(AssertionError):
@@ -371,3 +371,53 @@ def test_planted_transposed_gqa_map_is_caught(monkeypatch):
     monkeypatch.setattr(O, "forward", wrong)
     with pytest.raises(AssertionError):
         test_single_full_slice_matches_sdpa(64, 4, 2, 8)
+
+
+# ------------------------------------------------------------------------------------------
+# ALiBi score modification (Flex Attention paper, sections 2 and 3.1)
+# ------------------------------------------------------------------------------------------
+
+def test_alibi_matches_sdpa_with_additive_bias():
+    n, nk, d = 45, 38, 8
+    qr, kr, ty = W.random_slices(n, nk, 6, seed=9, p_dummy=0.0)
+    m = O.dense_mask(qr, kr, ty, n, nk)
+    rows = m.any(axis=1)
+    q, k, v = _rand((n, 4, d), 71), _rand((nk, 2, d), 72), _rand((nk, 2, d), 73)
+    slopes = [0.5, 0.25, 0.125, 0.0625]
+    o, l = O.forward(q, k, v, qr, kr, ty, softmax_scale=0.4, alibi_slopes=slopes)
+    i, j = np.meshgrid(np.arange(n), np.arange(nk), indexing="ij")
+    for h in range(4):
+        bias = slopes[h] * (j - i)
+        bias = np.where(m, bias, -np.inf)[rows]
+        qt = torch.tensor(q[rows][:, h])[None]
+        kt = torch.tensor(k[:, h // 2])[None]
+        vt = torch.tensor(v[:, h // 2])[None]
+        ro = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.tensor(bias)[None], scale=0.4)[0]
+        np.testing.assert_allclose(o[rows][:, h], ro.numpy(), atol=1e-12)
+        sc = 0.4 * (q[rows][:, h] @ k[:, h // 2].T) + bias
+        np.testing.assert_allclose(l[h, rows], torch.logsumexp(torch.tensor(sc), dim=-1).numpy(), atol=1e-12)
+
+
+def test_alibi_zero_slopes_is_identity_and_gradients_match_finite_differences():
+    n, d = 10, 4
+    q, k, v, do = _rand((n, 2, d), 81), _rand((n, 1, d), 82), _rand((n, 1, d), 83), _rand((n, 2, d), 84)
+    qr, kr, ty = [[0, 10]], [[0, 10]], [O.CAUSAL]
+    a = O.forward(q, k, v, qr, kr, ty, softcap=2.0)
+    b = O.forward(q, k, v, qr, kr, ty, softcap=2.0, alibi_slopes=[0.0, 0.0])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    slopes = [0.3, -0.2]
+    dq, dk, dv = O.backward(q, k, v, do, qr, kr, ty, softcap=2.0, alibi_slopes=slopes)
+
+    def loss():
+        o, _ = O.forward(q, k, v, qr, kr, ty, softcap=2.0, alibi_slopes=slopes)
+        return float(np.sum(o * do))
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps; fp = loss()
+            x[idx] = old - eps; fm = loss()
+            x[idx] = old
+            num[idx] = (fp - fm) / (2 * eps)
+        assert np.abs(num - g).max() / max(1e-12, np.abs(g).max()) < 1e-6
