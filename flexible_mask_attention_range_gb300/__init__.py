@@ -37,6 +37,11 @@ class FfaShape(ctypes.Structure):
                 ("head_dim", ctypes.c_int32)]
 
 
+class FfaOptions(ctypes.Structure):
+    _fields_ = [("alibi_slopes", ctypes.c_void_p), ("deterministic", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 7)]
+
+
 class FfaError(RuntimeError):
     pass
 
@@ -55,6 +60,10 @@ SIGNATURES = {
                                _SZ, _P, _P]),
     "ffa_bwd": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _F, _F,
                                _P, _P, _P, _P, _SZ, _P, _P]),
+    "ffa_fwd_ex": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _I32, _F, _F, _P, _P, _P,
+                                  _SZ, _P, _P, ctypes.POINTER(FfaOptions)]),
+    "ffa_bwd_ex": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _F, _F,
+                                  _P, _P, _P, _P, _SZ, _P, _P, ctypes.POINTER(FfaOptions)]),
     "ffa_plan_tiles": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _I32, _I32, _P, _P, _SZ, _P,
                                       _P]),
     "ffa_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _I32, _F, _F, _P, _P,
@@ -156,9 +165,10 @@ def ffa_build_info() -> str:
 def ffa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_ranges, attn_type_map,
             softmax_scale: Optional[float] = None, softcap: float = 0.0,
             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-            workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None
-            ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """out [Nq,Hq,d] bf16 and lse [Hq,Nq] float32 (natural log); see include/ffa.h."""
+            workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+            alibi_slopes: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """out [Nq,Hq,d] bf16 and lse [Hq,Nq] float32 (natural log); see include/ffa.h.
+    ``alibi_slopes`` (float32 [Hq]) adds slope_h * (key - query position) to the scores."""
     dev = q.device
     nq, hq, d = q.shape
     nk, hkv = k.shape[0], k.shape[1]
@@ -180,9 +190,16 @@ def ffa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_range
     if status is not None:
         _need(status, "status", torch.int32, dev)
     scale = -1.0 if softmax_scale is None else float(softmax_scale)
-    rc = lib().ffa_fwd(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty), R,
-                       scale, float(softcap), _ptr(out), _ptr(lse), _ptr(workspace),
-                       workspace.numel(), _ptr(status), _stream(dev))
+    if alibi_slopes is None:
+        rc = lib().ffa_fwd(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty), R,
+                           scale, float(softcap), _ptr(out), _ptr(lse), _ptr(workspace),
+                           workspace.numel(), _ptr(status), _stream(dev))
+    else:
+        _need(alibi_slopes, "alibi_slopes", torch.float32, dev, (hq,))
+        opts = FfaOptions(alibi_slopes.data_ptr())
+        rc = lib().ffa_fwd_ex(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty), R,
+                              scale, float(softcap), _ptr(out), _ptr(lse), _ptr(workspace),
+                              workspace.numel(), _ptr(status), _stream(dev), ctypes.byref(opts))
     _check(rc, "ffa_fwd")
     return out, lse
 
@@ -221,8 +238,10 @@ def ffa_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges,
 
 def ffa_bwd(q, k, v, out, lse, dout, q_ranges, k_ranges, attn_type_map,
             softmax_scale: Optional[float] = None, softcap: float = 0.0,
-            dq=None, dk=None, dv=None, workspace=None, status=None):
-    """Gradients (dq, dk, dv) of sum(out * dout); see include/ffa.h."""
+            dq=None, dk=None, dv=None, workspace=None, status=None, alibi_slopes=None,
+            deterministic: bool = False):
+    """Gradients (dq, dk, dv) of sum(out * dout); see include/ffa.h.  ``deterministic``
+    orders the dq additions so the results are bit-reproducible."""
     dev = q.device
     nq, hq, d = q.shape
     nk, hkv = k.shape[0], k.shape[1]
@@ -247,9 +266,18 @@ def ffa_bwd(q, k, v, out, lse, dout, q_ranges, k_ranges, attn_type_map,
     if status is not None:
         _need(status, "status", torch.int32, dev)
     scale = -1.0 if softmax_scale is None else float(softmax_scale)
-    rc = lib().ffa_bwd(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
-                       _ptr(qr), _ptr(kr), _ptr(ty), R, scale, float(softcap), _ptr(dq), _ptr(dk),
-                       _ptr(dv), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    if alibi_slopes is None and not deterministic:
+        rc = lib().ffa_bwd(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                           _ptr(qr), _ptr(kr), _ptr(ty), R, scale, float(softcap), _ptr(dq), _ptr(dk),
+                           _ptr(dv), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    else:
+        if alibi_slopes is not None:
+            _need(alibi_slopes, "alibi_slopes", torch.float32, dev, (hq,))
+        opts = FfaOptions(_ptr(alibi_slopes), 1 if deterministic else 0)
+        rc = lib().ffa_bwd_ex(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                              _ptr(qr), _ptr(kr), _ptr(ty), R, scale, float(softcap), _ptr(dq), _ptr(dk),
+                              _ptr(dv), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev),
+                              ctypes.byref(opts))
     _check(rc, "ffa_bwd")
     return dq, dk, dv
 

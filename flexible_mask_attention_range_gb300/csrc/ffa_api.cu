@@ -140,11 +140,31 @@ size_t ffa_bwd_workspace_size(const ffa_shape* s, int32_t n_ranges) {
   return make_layout(s->total_q, s->total_k, s->num_heads_q, s->num_heads_kv, s->head_dim, n_ranges).bwd_total;
 }
 
+namespace {
+int check_options(const ffa_options* o) {
+  if (o == nullptr) return FFA_OK;
+  for (int i = 0; i < 7; ++i)
+    if (o->reserved[i] != 0) return FFA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(o->alibi_slopes) & 3u) != 0) return FFA_ERR_INVALID_ARG;
+  return FFA_OK;
+}
+}  // namespace
+
 int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
             const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
             float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
             void* stream) {
+  return ffa_fwd_ex(shape, q, k, v, q_ranges, k_ranges, attn_type_map, n_ranges, softmax_scale, softcap, out, lse,
+                    workspace, workspace_bytes, status, stream, nullptr);
+}
+
+int ffa_fwd_ex(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
+               const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
+               float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+               void* stream, const ffa_options* options) {
   int rc = check_shape(shape, n_ranges);
+  if (rc != FFA_OK) return rc;
+  rc = check_options(options);
   if (rc != FFA_OK) return rc;
   if (std::isnan(softcap) || softcap < 0.0f) return FFA_ERR_INVALID_ARG;
   const int64_t nq = shape->total_q, nk = shape->total_k;
@@ -187,6 +207,7 @@ int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
   a.v = v;
   a.out = out;
   a.lse = lse;
+  a.alibi = options != nullptr ? options->alibi_slopes : nullptr;
   a.plan = pv;
   a.status = status;
   a.wait_limit_ns = wait_limit_ns();
@@ -197,7 +218,18 @@ int ffa_bwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
             const float* lse, const void* dout, const int32_t* q_ranges, const int32_t* k_ranges,
             const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale, float softcap, void* dq,
             void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  return ffa_bwd_ex(shape, q, k, v, out, lse, dout, q_ranges, k_ranges, attn_type_map, n_ranges, softmax_scale,
+                    softcap, dq, dk, dv, workspace, workspace_bytes, status, stream, nullptr);
+}
+
+int ffa_bwd_ex(const ffa_shape* shape, const void* q, const void* k, const void* v, const void* out,
+               const float* lse, const void* dout, const int32_t* q_ranges, const int32_t* k_ranges,
+               const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale, float softcap, void* dq,
+               void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* status, void* stream,
+               const ffa_options* options) {
   int rc = check_shape(shape, n_ranges);
+  if (rc != FFA_OK) return rc;
+  rc = check_options(options);
   if (rc != FFA_OK) return rc;
   if (std::isnan(softcap) || softcap < 0.0f) return FFA_ERR_INVALID_ARG;
   const int64_t nq = shape->total_q, nk = shape->total_k;
@@ -249,6 +281,15 @@ int ffa_bwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
   a.rowD = reinterpret_cast<float*>(wb + L.rowD);
   a.lse2 = reinterpret_cast<float*>(wb + L.lse2);
   a.dqacc = reinterpret_cast<float*>(wb + L.dqacc);
+  a.alibi = options != nullptr ? options->alibi_slopes : nullptr;
+  a.deterministic = (options != nullptr && options->deterministic) ? 1 : 0;
+  a.tile_rank = reinterpret_cast<int*>(wb + L.tile_rank);
+  a.dq_sem = reinterpret_cast<int*>(wb + L.dq_sem);
+  if (a.deterministic) {
+    if (launch_plan_ranks(P, pv, a.tile_rank, s) != cudaSuccess) return FFA_ERR_CUDA;
+    if (cudaMemsetAsync(a.dq_sem, 0, static_cast<size_t>(P.hq) * P.nqt * sizeof(int), s) != cudaSuccess)
+      return FFA_ERR_CUDA;
+  }
   a.plan = pv;
   a.status = status;
   a.wait_limit_ns = wait_limit_ns();

@@ -74,6 +74,10 @@ struct BwdParams {
   float* dqacc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  const float* alibi;  // per-query-head ALiBi slopes, or null
+  int det;              // deterministic dq: ordered additions, items by ascending key tile
+  const int* tile_rank;
+  int* dq_sem;
   int* status;
   uint64_t wait_limit_ns;
 };
@@ -142,9 +146,30 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Waits until *counter reaches `target` (another CTA's release), bounded like mbar_wait.
+__device__ bool wait_counter(const int* counter, int target, const volatile int* abort, uint64_t limit_ns) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+      if (ld_acquire_gpu(counter) >= target) return true;
+      __nanosleep(64);
+    }
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // A[m][k] K-major x B[n][k] K-major, both 128-row tiles of D columns (2 boxes when D = 128)
@@ -188,14 +213,14 @@ __device__ __forceinline__ BwdItem decode_item(const BwdParams& p, int item) {
   BwdItem it;
   const int rank = item / p.hkv;
   it.kvh = item - rank * p.hkv;
-  it.kt = p.plan.col_order[rank];
+  it.kt = p.det ? rank : p.plan.col_order[rank];  // deterministic: ascending key tiles
   it.n_ent = p.plan.col_cnt[it.kt];
   it.n_steps = it.n_ent * p.G;
   it.ents = p.plan.col_ent + static_cast<size_t>(it.kt) * p.nqt;
   return it;
 }
 
-template <int D, bool kCap>
+template <int D, bool kCap, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     ffa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -305,15 +330,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[4];
         const bool masked = (cls != FFA_TILE_FULL) || (qt * kTile + kTile > p.nq) || !in_keys;
         if (masked) key_mask(p, cls, j, qt, nsl, sl, w);
+        const float slope_log2 = kBias ? p.alibi[it.kvh * p.G + (t % p.G)] * kLog2e : 0.0f;
+        const float bbase = kBias ? slope_log2 * static_cast<float>(j - qt * kTile) : 0.0f;
         // phase 1: P^T of this warpgroup's 64 queries from S^T and the row LSEs; keep
         // P' = P (or P (1 - tanh^2) with softcap) packed as bf16 for phase 2
         uint32_t pp[32];
+        uint32_t sv2[2][32];  // both chunks in flight before the one wait
+        tmem_ld32(tS, sv2[0]);
+        tmem_ld32(tS + 32, sv2[1]);
+        tmem_wait_ld();
+        reg_fence(sv2[0]);
+        reg_fence(sv2[1]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t sv[32];
-          tmem_ld32(tS + 32 * c, sv);
-          tmem_wait_ld();
-          reg_fence(sv);
+          const uint32_t (&sv)[32] = sv2[c];
           uint32_t pk[16];
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
@@ -324,14 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h4 = 0; h4 < 4; ++h4) {
               const int col = c0 + 32 * c + 4 * k4 + h4;
               const float s = __uint_as_float(sv[4 * k4 + h4]);
+              // ALiBi (log2 domain): slope * log2(e) * (key j - query qt*128+col)
+              const float lb = kBias ? fmaf(-slope_log2, static_cast<float>(col), bbase) - lv[h4] : -lv[h4];
               float pr;
               if (kCap) {
                 const float x = capped_log2(s, p.cap_c, p.cap_k);
-                pr = ex2_approx(x - lv[h4]);
+                pr = ex2_approx(x + lb);
                 const float th = x * p.inv_cap_c;
                 pd[h4] = pr * (1.0f - th * th);
               } else {
-                pr = ex2_approx(fmaf(s, p.scale_log2, -lv[h4]));
+                pr = ex2_approx(fmaf(s, p.scale_log2, lb));
                 pd[h4] = pr;
               }
               if (masked && !((w[col >> 5] >> (col & 31)) & 1u)) {
@@ -362,12 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const float* Drow = stat + kTile;
+        uint32_t dv2[2][32];
+        tmem_ld32(tP, dv2[0]);
+        tmem_ld32(tP + 32, dv2[1]);
+        tmem_wait_ld();
+        reg_fence(dv2[0]);
+        reg_fence(dv2[1]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t dv[32];
-          tmem_ld32(tP + 32 * c, dv);
-          tmem_wait_ld();
-          reg_fence(dv);
+          const uint32_t (&dv)[32] = dv2[c];
           uint32_t pk[16];
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
@@ -449,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = named_bar_and(1, 128, mbar_wait(dq_full, step_cnt & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
+        bool turn = true;  // deterministic mode: this CTA's turn to add into (h, qt) came
 #pragma unroll
         for (int half = 0; half < D / 64; ++half) {
           uint32_t o[2][32];
@@ -480,13 +516,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
             if (leader) {
-              tma_reduce_add_2d(&tmDQ, buf, h * D + 32 * c, qt * kTile);
-              bulk_commit_group();
+              if (p.det && c == 0) {  // wait for the key tiles before this one in qt's list
+                turn = wait_counter(p.dq_sem + static_cast<size_t>(h) * p.nqt + qt,
+                                    p.tile_rank[static_cast<size_t>(qt) * p.nkt + it.kt], abort_flag, lim);
+                if (!turn) record_abort(abort_flag, p.status);
+                fence_proxy_async_global();
+              }
+              if (turn) {
+                tma_reduce_add_2d(&tmDQ, buf, h * D + 32 * c, qt * kTile);
+                bulk_commit_group();
+              }
             }
           }
         }
         if (leader) {
-          bulk_wait_group_read<0>();
+          if (p.det) {  // the additions must have landed before the next key tile may add
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            fence_proxy_async_global();
+            if (turn) red_release_gpu_add(p.dq_sem + static_cast<size_t>(h) * p.nqt + qt, 1);
+          } else {
+            bulk_wait_group_read<0>();
+          }
           mbar_arrive(sds_free);
         }
         ++step_cnt;
@@ -682,11 +732,11 @@ __global__ void __launch_bounds__(256) ffa_bwd_dq_convert(const float* __restric
   }
 }
 
-template <int D, bool kCap>
+template <int D, bool kCap, bool kBias>
 cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   using SM = BwdSmem<D>;
   static bool attr_set = false;
-  auto kern = ffa_bwd_kernel<D, kCap>;
+  auto kern = ffa_bwd_kernel<D, kCap, kBias>;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
     if (e != cudaSuccess) return e;
@@ -727,12 +777,24 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   p.dqacc = a.dqacc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.alibi = a.alibi;
+  p.det = a.deterministic;
+  p.tile_rank = a.tile_rank;
+  p.dq_sem = a.dq_sem;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
   const int grid = p.n_items < nsm ? p.n_items : nsm;
   if (grid > 0) {
     if (g_kernel_events.bwd_start != nullptr) cudaEventRecord(g_kernel_events.bwd_start, stream);
-    kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, mdo, mdq, p);
+    if (p.det) {
+      // CTAs wait on one another's dq additions: all of them must be resident at once
+      void* args[] = {&mq, &mk, &mv, &mdo, &mdq, &p};
+      cudaError_t le = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
+                                                   args, SM::kAlloc, stream);
+      if (le != cudaSuccess) return le;
+    } else {
+      kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, mdo, mdq, p);
+    }
     if (g_kernel_events.bwd_stop != nullptr) cudaEventRecord(g_kernel_events.bwd_stop, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -746,9 +808,13 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s) {
-  const bool cap = a.softcap > 0.0f;
-  if (a.P.d == 64) return cap ? launch_impl<64, true>(a, s) : launch_impl<64, false>(a, s);
-  return cap ? launch_impl<128, true>(a, s) : launch_impl<128, false>(a, s);
+  const bool cap = a.softcap > 0.0f, bias = a.alibi != nullptr;
+  if (a.P.d == 64) {
+    if (bias) return cap ? launch_impl<64, true, true>(a, s) : launch_impl<64, false, true>(a, s);
+    return cap ? launch_impl<64, true, false>(a, s) : launch_impl<64, false, false>(a, s);
+  }
+  if (bias) return cap ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
+  return cap ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
 }
 
 }  // namespace ffa

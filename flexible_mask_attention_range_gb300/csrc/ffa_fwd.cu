@@ -69,6 +69,7 @@ struct FwdParams {
   PlanView plan;
   __nv_bfloat16* out;
   float* lse;
+  const float* alibi;  // per-query-head ALiBi slopes, or null
   int* status;
   uint64_t wait_limit_ns;
 };
@@ -179,12 +180,13 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint3
   }
 }
 
-template <int D, bool kCap>
+template <int D, bool kCap, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using SM = FwdSmem<D>;
   constexpr int S = SM::kStages;
+  constexpr bool kPre = kCap || kBias;  // logits formed in the log2 domain before the row max
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sm = smem_raw + pad;
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const uint32_t* ents = it.ents;
+      const float slope_log2 = kBias ? p.alibi[h] * kLog2e : 0.0f;
       const int nsl = qt < p.nqt ? p.plan.row_nsl[qt] : 0;
       const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
       // l_run: sum of the fp32 p (for the LSE); r_run: sum of the bf16-rounded p that the PV
@@ -284,6 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence(sv[c]);
         const bool masked = (cls != FFA_TILE_FULL) || (kt * kTile + kTile > p.nk);
+        // ALiBi in the log2 domain: slope * log2(e) * (key - row) = bbase + slope * log2(e) * c
+        const float bbase = kBias ? slope_log2 * static_cast<float>(kt * kTile - row) : 0.0f;
         float mx = -INFINITY;
         if (masked) {
           uint32_t w[4];
@@ -292,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c) {
             float x = __uint_as_float(sv[c >> 5][c & 31]);
             if (kCap) x = capped_log2(x, p.cap_c, p.cap_k);
+            if (kBias) x = (kCap ? x : x * p.scale_log2) + fmaf(slope_log2, static_cast<float>(c), bbase);
             x = ((w[c >> 5] >> (c & 31)) & 1u) ? x : -INFINITY;
             sv[c >> 5][c & 31] = __float_as_uint(x);
             mx = fmaxf(mx, x);
@@ -300,14 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             float x = __uint_as_float(sv[c >> 5][c & 31]);
-            if (kCap) {
-              x = capped_log2(x, p.cap_c, p.cap_k);
-              sv[c >> 5][c & 31] = __float_as_uint(x);
-            }
+            if (kCap) x = capped_log2(x, p.cap_c, p.cap_k);
+            if (kBias) x = (kCap ? x : x * p.scale_log2) + fmaf(slope_log2, static_cast<float>(c), bbase);
+            if (kPre) sv[c >> 5][c & 31] = __float_as_uint(x);
             mx = fmaxf(mx, x);
           }
         }
-        const float m_tile = kCap ? mx : mx * p.scale_log2;
+        const float m_tile = kPre ? mx : mx * p.scale_log2;
         const bool need = m_tile > m_run + kTau;
         const bool rescale = need && (m_run != -INFINITY);
         const float alpha = rescale ? ex2_approx(m_run - m_tile) : 1.0f;
@@ -324,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const float x0 = __uint_as_float(sv[c4][2 * k]), x1 = __uint_as_float(sv[c4][2 * k + 1]);
-            const float p0 = kCap ? ex2_approx(x0 + neg_m) : ex2_approx(fmaf(x0, p.scale_log2, neg_m));
-            const float p1 = kCap ? ex2_approx(x1 + neg_m) : ex2_approx(fmaf(x1, p.scale_log2, neg_m));
+            const float p0 = kPre ? ex2_approx(x0 + neg_m) : ex2_approx(fmaf(x0, p.scale_log2, neg_m));
+            const float p1 = kPre ? ex2_approx(x1 + neg_m) : ex2_approx(fmaf(x1, p.scale_log2, neg_m));
             sum += p0 + p1;
             pk[k] = pack_bf16x2(p0, p1);
             sum_r += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xffff0000u);
@@ -603,11 +608,11 @@ __global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
   p.lse[static_cast<size_t>(h) * p.nq + row] = mx + lg2_approx(wsum) * kLn2;
 }
 
-template <int D, bool kCap>
+template <int D, bool kCap, bool kBias>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   using SM = FwdSmem<D>;
   static bool attr_set = false;
-  auto kern = ffa_fwd_kernel<D, kCap>;
+  auto kern = ffa_fwd_kernel<D, kCap, kBias>;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
     if (e != cudaSuccess) return e;
@@ -629,6 +634,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.plan = a.plan;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
+  p.alibi = a.alibi;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
   const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
@@ -645,9 +651,13 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
-  const bool cap = a.softcap > 0.0f;
-  if (a.P.d == 64) return cap ? launch_impl<64, true>(a, s) : launch_impl<64, false>(a, s);
-  return cap ? launch_impl<128, true>(a, s) : launch_impl<128, false>(a, s);
+  const bool cap = a.softcap > 0.0f, bias = a.alibi != nullptr;
+  if (a.P.d == 64) {
+    if (bias) return cap ? launch_impl<64, true, true>(a, s) : launch_impl<64, false, true>(a, s);
+    return cap ? launch_impl<64, true, false>(a, s) : launch_impl<64, false, false>(a, s);
+  }
+  if (bias) return cap ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
+  return cap ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
 }
 
 }  // namespace ffa

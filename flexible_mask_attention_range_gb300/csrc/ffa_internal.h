@@ -42,7 +42,7 @@ struct WsLayout {
   size_t row_nsl = 0, row_sl = 0, grp_cnt = 0, grp_ent = 0;
   size_t grp_nch = 0, grp_pslot = 0, chunks = 0, chunk_len = 0, chunk_order = 0, part_o = 0, part_lse = 0;
   size_t col_nsl = 0, col_sl = 0, col_cnt = 0, col_ent = 0, col_order = 0;
-  size_t rowD = 0, lse2 = 0, dqacc = 0;
+  size_t rowD = 0, lse2 = 0, dqacc = 0, tile_rank = 0, dq_sem = 0;
   size_t fwd_total = 0, bwd_total = 0;
 };
 
@@ -108,6 +108,8 @@ inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int 
   L.rowD = take(static_cast<size_t>(hq) * nqt * kTile * 4);
   L.lse2 = take(static_cast<size_t>(hq) * nqt * kTile * 4);
   L.dqacc = take(static_cast<size_t>(nq > 0 ? nq : 1) * hq * d * 4);
+  L.tile_rank = take(nqt * nkt * 4);                       // deterministic backward only
+  L.dq_sem = take(static_cast<size_t>(hq) * nqt * 4);
   L.bwd_total = o;
   return L;
 }
@@ -171,6 +173,7 @@ cudaError_t launch_plan_slices(const ProblemDims& P, const int32_t* q_ranges, co
                                const int32_t* types, int R, const PlanView& v, int32_t* status, cudaStream_t s);
 cudaError_t launch_plan_rows(const ProblemDims& P, const WsLayout& L, const PlanView& v, cudaStream_t s);
 cudaError_t launch_plan_cols(const ProblemDims& P, const PlanView& v, cudaStream_t s);
+cudaError_t launch_plan_ranks(const ProblemDims& P, const PlanView& v, int* tile_rank, cudaStream_t s);
 
 // Forward (ffa_fwd.cu)
 struct FwdArgs {
@@ -181,6 +184,7 @@ struct FwdArgs {
   const void *q, *k, *v;
   void* out;
   float* lse;
+  const float* alibi = nullptr;  // per-query-head ALiBi slopes (device) or null
   PlanView plan;
   int32_t* status;
   uint64_t wait_limit_ns;
@@ -197,6 +201,10 @@ struct BwdArgs {
   float* rowD;   // D_i = dO_i . O_i, [Hq, nqt*128], 0 beyond Nq
   float* lse2;   // LSE_i * log2(e), [Hq, nqt*128], +inf for empty rows and beyond Nq
   float* dqacc;  // float32 [Nq, Hq, d]
+  const float* alibi = nullptr;
+  int deterministic = 0;
+  int* tile_rank = nullptr;  // [nqt, nkt]: position of key tile kt in query tile qt's list
+  int* dq_sem = nullptr;     // [Hq, nqt]: dq contributions added so far
   PlanView plan;
   int32_t* status;
   uint64_t wait_limit_ns;

@@ -333,7 +333,29 @@ __global__ void __launch_bounds__(1024) plan_chunks_kernel(int ngrp, int split_l
   counting_sort_desc(v.chunk_len, base, split_len, v.chunk_order, hist, warp_buf);
 }
 
+// ---------------------------------------------------------------- 4. ranks (deterministic bwd)
+// One block per query tile: tile_rank[qt][kt] = number of non-empty tiles (qt, kt' < kt).
+__global__ void __launch_bounds__(256) plan_ranks_kernel(ProblemDims P, PlanView v, int* __restrict__ rank) {
+  __shared__ int warp_buf[32];
+  const int qt = blockIdx.x;
+  int base = 0;
+  for (int c = 0; c < P.nkt; c += blockDim.x) {
+    const int kt = c + threadIdx.x;
+    const int ne = (kt < P.nkt && v.cls[static_cast<size_t>(qt) * P.nkt + kt] != 0) ? 1 : 0;
+    int total;
+    const int pos = base + block_exclusive_scan(ne, warp_buf, &total);
+    if (kt < P.nkt) rank[static_cast<size_t>(qt) * P.nkt + kt] = pos;
+    base += total;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_plan_ranks(const ProblemDims& P, const PlanView& v, int* tile_rank, cudaStream_t s) {
+  if (P.nqt == 0) return cudaSuccess;
+  plan_ranks_kernel<<<P.nqt, 256, 0, s>>>(P, v, tile_rank);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_plan_slices(const ProblemDims& P, const int32_t* q_ranges, const int32_t* k_ranges,
                                const int32_t* types, int R, const PlanView& v, int32_t* status, cudaStream_t s) {

@@ -133,6 +133,42 @@ int ffa_bwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
             void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * Optional score modification and future options for ffa_fwd_ex / ffa_bwd_ex.  A
+ * zero-initialised struct (or a NULL pointer) means: none.
+ *   alibi_slopes  device float32 [Hq] or NULL.  Adds slope_h * (j - i) to the (softcapped)
+ *                 score of query position i and key position j (packed token indices; for
+ *                 two tokens of one document this is their in-document distance): the ALiBi
+ *                 distance bias, a score modification of the Flex Attention paper
+ *                 (sections 2 and 3.1).  The bias enters the softmax only; it has no
+ *                 gradient.  Pass the same slopes to the forward and backward calls.
+ *   deterministic backward only.  Nonzero: each query tile's dq receives the contributions of
+ *                 its key tiles in ascending key-tile order (a per-(head, query tile)
+ *                 counter orders the float32 additions), so dq, dk and dv are bit-identical
+ *                 from run to run and under appended start == end slices.  The backward
+ *                 kernel then runs as a cooperative launch over key tiles in ascending
+ *                 order; waits on the counters are bounded (FFA_STATUS_TIMEOUT).
+ *   reserved      must be zero.
+ */
+typedef struct ffa_options {
+  const float* alibi_slopes;
+  int32_t deterministic;
+  int32_t reserved[7];
+} ffa_options;
+
+/* ffa_fwd with options (NULL options: identical to ffa_fwd). */
+int ffa_fwd_ex(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
+               const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
+               float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+               void* stream, const ffa_options* options);
+
+/* ffa_bwd with options (NULL options: identical to ffa_bwd). */
+int ffa_bwd_ex(const ffa_shape* shape, const void* q, const void* k, const void* v, const void* out,
+               const float* lse, const void* dout, const int32_t* q_ranges, const int32_t* k_ranges,
+               const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale, float softcap, void* dq,
+               void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* status, void* stream,
+               const ffa_options* options);
+
+/*
  * The planner alone: classify every tile of the global 128 x 128 tile grid as
  * FFA_TILE_EMPTY / PARTIAL / FULL under the union of the slices (block classification of
  * the Flex Attention paper, section 4, "Block Sparsity" / "Full Block Optimization"),

@@ -159,3 +159,63 @@ def test_long_causal_full_size_sampled_and_sum_property():
     assert float((dvs - dos).abs().max()) <= 1e-2 * float(dos.abs().max()) + 1.0
     dks = dk.double().sum(0).cpu()
     assert float(dks.abs().max()) < 2.0
+
+
+@pytest.mark.parametrize("nq,nk,hq,hkv,d,cap,seed", [(300, 300, 4, 2, 64, 0.0, 51), (513, 700, 6, 3, 128, 5.0, 52),
+                                                      (64, 9000, 2, 1, 128, 0.0, 53)])
+def test_alibi_score_modification(nq, nk, hq, hkv, d, cap, seed):
+    q, k, v, do = _draw(nq, nk, hq, hkv, d, seed)
+    qr, kr, ty = W.random_slices(nq, nk, 9, seed=seed)
+    # slopes 2^-5 .. : with the strongest ALiBi slopes (0.5) these masks make one key the
+    # nearest visible key of many rows and |dv| reaches ~17, where bf16 storage alone costs
+    # 0.06 of the absolute 5e-2 bound; these slopes keep |dv| <= 4
+    slopes = [2.0 ** (-(h + 5)) for h in range(hq)]
+    al = torch.tensor(slopes, dtype=torch.float32, device="cuda")
+    qc, kc, vc, dc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    out, lse = ffa.ffa_fwd(qc, kc, vc, qr, kr, ty, softcap=cap, alibi_slopes=al)
+    dq, dk, dv = ffa.ffa_bwd(qc, kc, vc, out, lse, dc, qr, kr, ty, softcap=cap, alibi_slopes=al)
+    torch.cuda.synchronize()
+    rq, rk, rv = O.backward(q, k, v, do, qr, kr, ty, softcap=cap, alibi_slopes=slopes)
+    assert_grad_close(to64(dq), rq, "dq")
+    assert_grad_close(to64(dk), rk, "dk")
+    assert_grad_close(to64(dv), rv, "dv")
+
+
+@pytest.mark.parametrize("name", ["tiny_256", "page1_2048_gqa"])
+def test_deterministic_backward_is_bit_reproducible_and_padding_invariant(name):
+    w = W.get(name)
+    q, k, v, do = (t.cuda() for t in W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed))
+    out, lse = ffa.ffa_fwd(q, k, v, w.q_ranges, w.k_ranges, w.types, w.softmax_scale)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = ffa.ffa_bwd(q, k, v, out, lse, do, w.q_ranges, w.k_ranges, w.types, w.softmax_scale, deterministic=True,
+                    status=st)
+    b = ffa.ffa_bwd(q, k, v, out, lse, do, w.q_ranges, w.k_ranges, w.types, w.softmax_scale, deterministic=True)
+    wp = w.padded()
+    c = ffa.ffa_bwd(q, k, v, out, lse, do, wp.q_ranges, wp.k_ranges, wp.types, w.softmax_scale, deterministic=True)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for x, y, z in zip(a, b, c):
+        assert torch.equal(x, y) and torch.equal(x, z)
+    rq, rk, rv = O.backward(q.cpu(), k.cpu(), v.cpu(), do.cpu(), w.q_ranges, w.k_ranges, w.types,
+                            softmax_scale=w.softmax_scale)
+    assert_grad_close(to64(a[0]), rq, "dq")
+    assert_grad_close(to64(a[1]), rk, "dk")
+    assert_grad_close(to64(a[2]), rv, "dv")
+
+
+@pytest.mark.parametrize("nq,nk,hq,hkv,d,R,cap,seed", [(700, 513, 6, 3, 64, 20, 0.0, 6),
+                                                        (1000, 1000, 8, 8, 128, 40, 2.0, 7)])
+def test_deterministic_backward_random(nq, nk, hq, hkv, d, R, cap, seed):
+    q, k, v, do = _draw(nq, nk, hq, hkv, d, seed)
+    qr, kr, ty = W.random_slices(nq, nk, R, seed=seed)
+    qc, kc, vc, dc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    out, lse = ffa.ffa_fwd(qc, kc, vc, qr, kr, ty, softcap=cap)
+    g1 = ffa.ffa_bwd(qc, kc, vc, out, lse, dc, qr, kr, ty, softcap=cap, deterministic=True)
+    g2 = ffa.ffa_bwd(qc, kc, vc, out, lse, dc, qr, kr, ty, softcap=cap, deterministic=True)
+    torch.cuda.synchronize()
+    for x, y in zip(g1, g2):
+        assert torch.equal(x, y)
+    rq, rk, rv = O.backward(q, k, v, do, qr, kr, ty, softcap=cap)
+    assert_grad_close(to64(g1[0]), rq, "dq")
+    assert_grad_close(to64(g1[1]), rk, "dk")
+    assert_grad_close(to64(g1[2]), rv, "dv")

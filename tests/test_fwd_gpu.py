@@ -179,3 +179,25 @@ def test_full_size_sampled_rows(name):
     # properties at every row: finite outputs, finite LSE (every row sees at least one key)
     assert torch.isfinite(out.float()).all()
     assert torch.isfinite(lse).all()
+
+
+ALIBI = [
+    # nq, nk, hq, hkv, d, cap, seed
+    (300, 300, 4, 2, 64, 0.0, 51),
+    (513, 700, 6, 3, 128, 5.0, 52),
+    (64, 9000, 2, 1, 128, 0.0, 53),      # split rows + merge
+    (1000, 1000, 8, 8, 128, 0.0, 54),
+]
+
+
+@pytest.mark.parametrize("nq,nk,hq,hkv,d,cap,seed", ALIBI)
+def test_alibi_score_modification(nq, nk, hq, hkv, d, cap, seed):
+    q, k, v, _ = _draw2(nq, nk, hq, hkv, d, seed)
+    qr, kr, ty = W.random_slices(nq, nk, 9, seed=seed)
+    slopes = [2.0 ** (-(h + 1)) for h in range(hq)]
+    out, lse = ffa.ffa_fwd(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, softcap=cap,
+                           alibi_slopes=torch.tensor(slopes, dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    ro, rl = O.forward(q, k, v, qr, kr, ty, softcap=cap, alibi_slopes=slopes)
+    assert_out_close(to64(out), ro)
+    assert_lse_close(to64(lse), rl)
