@@ -213,14 +213,14 @@ __device__ __forceinline__ BwdItem decode_item(const BwdParams& p, int item) {
   BwdItem it;
   const int rank = item / p.hkv;
   it.kvh = item - rank * p.hkv;
-  it.kt = p.det ? rank : p.plan.col_order[rank];  // deterministic: ascending key tiles
+  it.kt = p.det ? rank : p.plan.col_order[rank];  // deterministic: ascending key tiles (p.det == kDet)
   it.n_ent = p.plan.col_cnt[it.kt];
   it.n_steps = it.n_ent * p.G;
   it.ents = p.plan.col_ent + static_cast<size_t>(it.kt) * p.nqt;
   return it;
 }
 
-template <int D, bool kCap, bool kBias>
+template <int D, bool kCap, bool kBias, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1)
     ffa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -335,15 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // phase 1: P^T of this warpgroup's 64 queries from S^T and the row LSEs; keep
         // P' = P (or P (1 - tanh^2) with softcap) packed as bf16 for phase 2
         uint32_t pp[32];
-        uint32_t sv2[2][32];  // both chunks in flight before the one wait
-        tmem_ld32(tS, sv2[0]);
-        tmem_ld32(tS + 32, sv2[1]);
-        tmem_wait_ld();
-        reg_fence(sv2[0]);
-        reg_fence(sv2[1]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t (&sv)[32] = sv2[c];
+          uint32_t sv[32];
+          tmem_ld32(tS + 32 * c, sv);
+          tmem_wait_ld();
+          reg_fence(sv);
           uint32_t pk[16];
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
@@ -394,15 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const float* Drow = stat + kTile;
-        uint32_t dv2[2][32];
-        tmem_ld32(tP, dv2[0]);
-        tmem_ld32(tP + 32, dv2[1]);
-        tmem_wait_ld();
-        reg_fence(dv2[0]);
-        reg_fence(dv2[1]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t (&dv)[32] = dv2[c];
+          uint32_t dv[32];
+          tmem_ld32(tP + 32 * c, dv);
+          tmem_wait_ld();
+          reg_fence(dv);
           uint32_t pk[16];
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
@@ -516,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
             if (leader) {
-              if (p.det && c == 0) {  // wait for the key tiles before this one in qt's list
+              if (kDet && c == 0) {  // wait for the key tiles before this one in qt's list
                 turn = wait_counter(p.dq_sem + static_cast<size_t>(h) * p.nqt + qt,
                                     p.tile_rank[static_cast<size_t>(qt) * p.nkt + it.kt], abort_flag, lim);
                 if (!turn) record_abort(abort_flag, p.status);
@@ -530,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (leader) {
-          if (p.det) {  // the additions must have landed before the next key tile may add
+          if (kDet) {  // the additions must have landed before the next key tile may add
             asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
             fence_proxy_async_global();
             if (turn) red_release_gpu_add(p.dq_sem + static_cast<size_t>(h) * p.nqt + qt, 1);
@@ -732,11 +726,11 @@ __global__ void __launch_bounds__(256) ffa_bwd_dq_convert(const float* __restric
   }
 }
 
-template <int D, bool kCap, bool kBias>
+template <int D, bool kCap, bool kBias, bool kDet>
 cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   using SM = BwdSmem<D>;
   static bool attr_set = false;
-  auto kern = ffa_bwd_kernel<D, kCap, kBias>;
+  auto kern = ffa_bwd_kernel<D, kCap, kBias, kDet>;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
     if (e != cudaSuccess) return e;
@@ -786,7 +780,7 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   const int grid = p.n_items < nsm ? p.n_items : nsm;
   if (grid > 0) {
     if (g_kernel_events.bwd_start != nullptr) cudaEventRecord(g_kernel_events.bwd_start, stream);
-    if (p.det) {
+    if (kDet) {
       // CTAs wait on one another's dq additions: all of them must be resident at once
       void* args[] = {&mq, &mk, &mv, &mdo, &mdq, &p};
       cudaError_t le = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
@@ -807,14 +801,19 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+template <int D, bool kCap, bool kBias>
+cudaError_t launch_det(const BwdArgs& a, cudaStream_t s) {
+  return a.deterministic ? launch_impl<D, kCap, kBias, true>(a, s) : launch_impl<D, kCap, kBias, false>(a, s);
+}
+
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s) {
   const bool cap = a.softcap > 0.0f, bias = a.alibi != nullptr;
   if (a.P.d == 64) {
-    if (bias) return cap ? launch_impl<64, true, true>(a, s) : launch_impl<64, false, true>(a, s);
-    return cap ? launch_impl<64, true, false>(a, s) : launch_impl<64, false, false>(a, s);
+    if (bias) return cap ? launch_det<64, true, true>(a, s) : launch_det<64, false, true>(a, s);
+    return cap ? launch_det<64, true, false>(a, s) : launch_det<64, false, false>(a, s);
   }
-  if (bias) return cap ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
-  return cap ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
+  if (bias) return cap ? launch_det<128, true, true>(a, s) : launch_det<128, false, true>(a, s);
+  return cap ? launch_det<128, true, false>(a, s) : launch_det<128, false, false>(a, s);
 }
 
 }  // namespace ffa

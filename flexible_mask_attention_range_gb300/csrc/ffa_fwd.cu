@@ -153,6 +153,44 @@ __device__ __forceinline__ void row_mask(const FwdParams& p, int cls, int row, i
   }
 }
 
+// The keys visible to query row `row` as at most two disjoint intervals (the union of the
+// row's slices, merged).  Returns false when the union needs more than two intervals.
+__device__ __forceinline__ bool row_intervals(const FwdParams& p, int row, int nsl, const int* sl, int& lo0,
+                                              int& hi0, int& lo1, int& hi1) {
+  lo0 = hi0 = lo1 = hi1 = 0;
+  int n_ivl = 0;
+  const int n = nsl >= 0 ? nsl : p.plan.hdr[0];
+  for (int k = 0; k < n; ++k) {
+    const int si = nsl >= 0 ? sl[k] : k;
+    const int4 s = p.plan.slices[si];
+    if (row < s.x || row >= s.y) continue;
+    const int lo = s.z;
+    const int hi = (p.plan.stypes[si] == FFA_CAUSAL) ? min(s.w, row + s.w - s.y + 1) : s.w;
+    if (lo >= hi) continue;
+    // merge with an existing interval when they overlap or touch
+    if (n_ivl > 0 && lo <= hi0 && hi >= lo0) {
+      lo0 = min(lo0, lo);
+      hi0 = max(hi0, hi);
+    } else if (n_ivl > 1 && lo <= hi1 && hi >= lo1) {
+      lo1 = min(lo1, lo);
+      hi1 = max(hi1, hi);
+    } else if (n_ivl == 0) {
+      lo0 = lo; hi0 = hi; n_ivl = 1;
+    } else if (n_ivl == 1) {
+      lo1 = lo; hi1 = hi; n_ivl = 2;
+    } else {
+      return false;
+    }
+    if (n_ivl == 2 && lo0 <= hi1 && hi0 >= lo1) {  // the two became one
+      lo0 = min(lo0, lo1);
+      hi0 = max(hi0, hi1);
+      lo1 = hi1 = 0;
+      n_ivl = 1;
+    }
+  }
+  return true;
+}
+
 // tanh(y) * C in the log2 domain from one exp2 and one reciprocal:
 // tanh(y) = 1 - 2 / (1 + e^{2y}); e^{2y} = 2^{s * cap_k}.
 __device__ __forceinline__ float capped_log2(float s, float cap_c, float cap_k) {
@@ -268,12 +306,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float slope_log2 = kBias ? p.alibi[h] * kLog2e : 0.0f;
       const int nsl = qt < p.nqt ? p.plan.row_nsl[qt] : 0;
       const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
+      // this row's visible keys once per item; PARTIAL tiles clip them instead of rereading
+      // the slice list (rows whose union needs more than two intervals use the list)
+      int ilo0, ihi0, ilo1, ihi1;
+      const bool ivl_ok = row_intervals(p, row, nsl, sl, ilo0, ihi0, ilo1, ihi1);
+      uint32_t e_next = ents[0];
       // l_run: sum of the fp32 p (for the LSE); r_run: sum of the bf16-rounded p that the PV
       // MMA actually multiplies (normalising O by it keeps the weights a convex combination,
       // so a dominant key is reproduced exactly even when the reference max is stale)
       float m_run = -INFINITY, l_run = 0.0f, r_run = 0.0f;
       for (int j = 0; j < n; ++j) {
-        const uint32_t e = ents[j];
+        const uint32_t e = e_next;
+        if (j + 1 < n) e_next = ents[j + 1];  // in flight while this tile is processed
         const int kt = entry_idx(e);
         const int cls = entry_cls(e, wg);
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], s_cnt & 1u, abort_flag, lim));
@@ -292,7 +336,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mx = -INFINITY;
         if (masked) {
           uint32_t w[4];
-          row_mask(p, cls, row, kt, nsl, sl, w);
+          if (ivl_ok && cls != FFA_TILE_FULL) {
+            const int c0 = kt * kTile;
+            w[0] = w[1] = w[2] = w[3] = 0u;
+            if (cls == FFA_TILE_PARTIAL) {
+              set_bits(w, max(ilo0 - c0, 0), min(ihi0 - c0, kTile));
+              set_bits(w, max(ilo1 - c0, 0), min(ihi1 - c0, kTile));
+            }
+            const int valid = p.nk - c0;
+            if (valid < kTile) {
+              uint32_t t4[4] = {0u, 0u, 0u, 0u};
+              set_bits(t4, 0, valid);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) w[k] &= t4[k];
+            }
+          } else {
+            row_mask(p, cls, row, kt, nsl, sl, w);
+          }
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             float x = __uint_as_float(sv[c >> 5][c & 31]);
