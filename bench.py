@@ -363,6 +363,10 @@ def oracle_sample(w: W.Workload, inputs, rows: np.ndarray):
     return dt, flops
 
 
+# about 10-20 s of float64 oracle work on the 64K workload (roughly 0.1 s per sampled row)
+CPU_BASELINE_ROWS = 128
+
+
 def cpu_threads() -> int:
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var, "").isdigit():
@@ -377,7 +381,7 @@ def sample_rows(w: W.Workload, n: int, seed: int):
 
 def run_reference(args, w: W.Workload):
     inputs = make_inputs(w)[:4]
-    rows_per_step = 6
+    rows_per_step = 24
     for i in range(args.warmup):
         oracle_sample(w, inputs, sample_rows(w, rows_per_step, 1000 + i))
     times, flops = [], []
@@ -421,12 +425,13 @@ def main():
     result, inputs = run_ours(args, w, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            rows = sample_rows(w, 8, 77)
+            n_rows = CPU_BASELINE_ROWS
+            rows = sample_rows(w, n_rows, 77)
             dt, fl = oracle_sample(w, inputs, rows)
             result["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": UNIT, "cores": cpu_threads(),
                                       "kind": "oracle", "seconds": round(dt, 2),
-                                      "sample": "8 random query rows (forward + dq over each row's full key "
-                                                "set, all heads), float64 numpy"}
+                                      "sample": f"{n_rows} random query rows (forward + dq over each row's "
+                                                "full key set, all heads), float64 numpy"}
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist
