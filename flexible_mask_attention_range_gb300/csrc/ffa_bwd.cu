@@ -26,6 +26,7 @@
 // dS^T of half h over [128+64h, 128+64h+32), then dQ [128,128+D); dV [256,256+D),
 // dK [256+D,256+2D).
 #include <algorithm>
+#include <type_traits>
 
 #include "ffa_internal.h"
 #include "ffa_ptx.cuh"
@@ -335,6 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // phase 1: P^T of this warpgroup's 64 queries from S^T and the row LSEs; keep
         // P' = P (or P (1 - tanh^2) with softcap) packed as bf16 for phase 2
         uint32_t pp[32];
+        // kM: this tile may hide elements (mk says whether it does).  Without softcap the loop
+        // exists twice so fully visible tiles carry no per-element mask test; with softcap one
+        // copy is kept (a second one costs registers there).
+        auto p1_body = [&](auto mtag, bool mk) {
+        constexpr bool kM = decltype(mtag)::value;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sv[32];
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pr = ex2_approx(fmaf(s, p.scale_log2, lb));
                 pd[h4] = pr;
               }
-              if (masked && !((w[col >> 5] >> (col & 31)) & 1u)) {
+              if (kM && mk && !((w[col >> 5] >> (col & 31)) & 1u)) {
                 pr = 0.0f;
                 pd[h4] = 0.0f;
               }
@@ -380,6 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tmem_st16(tS + 16 * c, pk);
+        }
+        };
+        if (kCap) {
+          p1_body(std::true_type{}, masked);
+        } else if (masked) {
+          p1_body(std::true_type{}, true);
+        } else {
+          p1_body(std::false_type{}, false);
         }
         tmem_wait_st();
         tc_fence_before();

@@ -333,7 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool masked = (cls != FFA_TILE_FULL) || (kt * kTile + kTile > p.nk);
         // ALiBi in the log2 domain: slope * log2(e) * (key - row) = bbase + slope * log2(e) * c
         const float bbase = kBias ? slope_log2 * static_cast<float>(kt * kTile - row) : 0.0f;
-        float mx = -INFINITY;
+        // row max: eight independent partial maxima when the logits are formed first (a
+        // longer transform per element), one chain otherwise (measured faster there)
+        constexpr int kMx = kPre ? 8 : 1;
+        float mxs[kMx];
+#pragma unroll
+        for (int u = 0; u < kMx; ++u) mxs[u] = -INFINITY;
         if (masked) {
           uint32_t w[4];
           if (ivl_ok && cls != FFA_TILE_FULL) {
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kBias) x = (kCap ? x : x * p.scale_log2) + fmaf(slope_log2, static_cast<float>(c), bbase);
             x = ((w[c >> 5] >> (c & 31)) & 1u) ? x : -INFINITY;
             sv[c >> 5][c & 31] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
+            mxs[c % kMx] = fmaxf(mxs[c % kMx], x);
           }
         } else {
 #pragma unroll
@@ -369,9 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kCap) x = capped_log2(x, p.cap_c, p.cap_k);
             if (kBias) x = (kCap ? x : x * p.scale_log2) + fmaf(slope_log2, static_cast<float>(c), bbase);
             if (kPre) sv[c >> 5][c & 31] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
+            mxs[c % kMx] = fmaxf(mxs[c % kMx], x);
           }
         }
+        float mx = mxs[0];
+#pragma unroll
+        for (int u = 1; u < kMx; ++u) mx = fmaxf(mx, mxs[u]);
         const float m_tile = kPre ? mx : mx * p.scale_log2;
         const bool need = m_tile > m_run + kTau;
         const bool rescale = need && (m_run != -INFINITY);
@@ -382,23 +390,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           r_run *= alpha;
         }
         const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
-        float sum = 0.0f, sum_r = 0.0f;
+        // exponentials two columns at a time: the argument and both running sums use packed
+        // fp32 pair instructions; two accumulator pairs each shorten the addition chains
+        float2 sum2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+        float2 sumr2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+        const float sc = kPre ? 1.0f : p.scale_log2;
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float x0 = __uint_as_float(sv[c4][2 * k]), x1 = __uint_as_float(sv[c4][2 * k + 1]);
-            const float p0 = kPre ? ex2_approx(x0 + neg_m) : ex2_approx(fmaf(x0, p.scale_log2, neg_m));
-            const float p1 = kPre ? ex2_approx(x1 + neg_m) : ex2_approx(fmaf(x1, p.scale_log2, neg_m));
-            sum += p0 + p1;
+            const float2 y = fma2(make_float2(__uint_as_float(sv[c4][2 * k]), __uint_as_float(sv[c4][2 * k + 1])), sc2,
+                                  nm2);
+            const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+            sum2[k & 1] = add2(sum2[k & 1], make_float2(p0, p1));
             pk[k] = pack_bf16x2(p0, p1);
-            sum_r += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xffff0000u);
+            sumr2[k & 1] = add2(sumr2[k & 1], make_float2(__uint_as_float(pk[k] << 16),
+                                                          __uint_as_float(pk[k] & 0xffff0000u)));
           }
           tmem_st16(tS + 16 * c4, pk);
         }
-        l_run += sum;
-        r_run += sum_r;
+        l_run += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
+        r_run += (sumr2[0].x + sumr2[0].y) + (sumr2[1].x + sumr2[1].y);
         // Rescale this row of O when its reference max moved.  O is stable here: the S MMA
         // that produced this tile was issued after the previous PV MMA, and the next PV MMA
         // waits for this warpgroup's p_full arrival below.
