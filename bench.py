@@ -319,15 +319,20 @@ GPU_LAUNCHES_PER_STEP = 4 + 6
 
 
 def read_profile_traffic(workload: str):
-    """Per-launch DRAM bytes of the main kernels from the committed ncu summary, if any."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """Per-launch DRAM bytes of the main kernels from the committed ncu summary table
+    (profiles/traffic.md rows `| workload | kernel | bytes |`), if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    out = {}
     if not os.path.exists(p):
-        return {}
-    try:
-        d = json.load(open(p))
-        return d.get(workload, {})
-    except Exception:
-        return {}
+        return out
+    for line in open(p):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) == 3 and cells[0] == workload:
+            try:
+                out[cells[1]] = float(cells[2])
+            except ValueError:
+                pass
+    return out
 
 
 def oracle_sample(w: W.Workload, inputs, rows: np.ndarray):
