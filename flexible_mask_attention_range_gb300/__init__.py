@@ -26,6 +26,7 @@ TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 STATUS_BAD_RANGE = 1
 STATUS_TIMEOUT = 2
 STATUS_SMEM = 4
+STATUS_BAD_PAGE = 8
 FWD_NOALLOC_SCRATCH_BYTES = 8 << 20
 ERR_TOO_LARGE = 5
 TILE = 128
@@ -66,6 +67,8 @@ SIGNATURES = {
                                   _P, _P, _P, _P, _SZ, _P, _P, ctypes.POINTER(FfaOptions)]),
     "ffa_plan_tiles": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _I32, _I32, _P, _P, _SZ, _P,
                                       _P]),
+    "ffa_fwd_paged": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _I32, ctypes.c_int64, _P, _P, _P,
+                                     _I32, _F, _F, _P, _P, _P, _SZ, _P, _P, ctypes.POINTER(FfaOptions)]),
     "ffa_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _I32, _F, _F, _P, _P,
                                        _P, _P]),
     "ffa_set_kernel_events": (ctypes.c_int, [_P, _P, _P, _P]),
@@ -201,6 +204,50 @@ def ffa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_range
                               scale, float(softcap), _ptr(out), _ptr(lse), _ptr(workspace),
                               workspace.numel(), _ptr(status), _stream(dev), ctypes.byref(opts))
     _check(rc, "ffa_fwd")
+    return out, lse
+
+
+def ffa_fwd_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, page_table: torch.Tensor,
+                  total_k: int, q_ranges, k_ranges, attn_type_map, softmax_scale: Optional[float] = None,
+                  softcap: float = 0.0, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                  alibi_slopes: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """ffa_fwd over a paged key/value cache: ``k_pages``/``v_pages`` are bf16
+    [n_pages, page_size, Hkv, d] pools and ``page_table`` (int32 [ceil(total_k / page_size)])
+    maps each logical page of the ``total_k`` keys to a physical page; ranges, masks and
+    results use logical positions (see include/ffa.h)."""
+    dev = q.device
+    nq, hq, d = q.shape
+    n_pages, page_size, hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k_pages, "k_pages", torch.bfloat16, dev, (n_pages, page_size, hkv, d))
+    _need(v_pages, "v_pages", torch.bfloat16, dev, (n_pages, page_size, hkv, d))
+    n_lp = (int(total_k) + page_size - 1) // page_size
+    _need(page_table, "page_table", torch.int32, dev, (n_lp,))
+    qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
+    if out is None:
+        out = torch.empty(nq, hq, d, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(hq, nq, dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev, (nq, hq, d))
+    _need(lse, "lse", torch.float32, dev, (hq, nq))
+    R = qr.shape[0]
+    shp = _shape(nq, int(total_k), hq, hkv, d)
+    ws_bytes = int(lib().ffa_fwd_workspace_size(ctypes.byref(shp), R))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    scale = -1.0 if softmax_scale is None else float(softmax_scale)
+    opts = None
+    if alibi_slopes is not None:
+        _need(alibi_slopes, "alibi_slopes", torch.float32, dev, (hq,))
+        opts = FfaOptions(alibi_slopes.data_ptr())
+    rc = lib().ffa_fwd_paged(ctypes.byref(shp), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                             int(page_size), int(n_pages), _ptr(qr), _ptr(kr), _ptr(ty), R, scale, float(softcap),
+                             _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev),
+                             ctypes.byref(opts) if opts is not None else None)
+    _check(rc, "ffa_fwd_paged")
     return out, lse
 
 

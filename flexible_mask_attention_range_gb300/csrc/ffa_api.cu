@@ -158,10 +158,49 @@ int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
                     workspace, workspace_bytes, status, stream, nullptr);
 }
 
+namespace {
+struct PagedKV {
+  const int32_t* page_table = nullptr;
+  int page_size = 0;
+  int64_t n_pages = 0;
+};
+
+int fwd_common(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
+               const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
+               float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+               void* stream, const ffa_options* options, const PagedKV& pg);
+}  // namespace
+
 int ffa_fwd_ex(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
                const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
                float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
                void* stream, const ffa_options* options) {
+  return fwd_common(shape, q, k, v, q_ranges, k_ranges, attn_type_map, n_ranges, softmax_scale, softcap, out, lse,
+                    workspace, workspace_bytes, status, stream, options, PagedKV{});
+}
+
+int ffa_fwd_paged(const ffa_shape* shape, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* page_table, int32_t page_size, int64_t n_pages, const int32_t* q_ranges,
+                  const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
+                  float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+                  void* stream, const ffa_options* options) {
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FFA_ERR_INVALID_ARG;
+  if (n_pages < 1 || n_pages * static_cast<int64_t>(page_size) >= (static_cast<int64_t>(1) << 31))
+    return FFA_ERR_INVALID_ARG;
+  if (shape != nullptr && shape->total_k > 0 && page_table == nullptr) return FFA_ERR_INVALID_ARG;
+  PagedKV pg;
+  pg.page_table = page_table;
+  pg.page_size = page_size;
+  pg.n_pages = n_pages;
+  return fwd_common(shape, q, k_pages, v_pages, q_ranges, k_ranges, attn_type_map, n_ranges, softmax_scale, softcap,
+                    out, lse, workspace, workspace_bytes, status, stream, options, pg);
+}
+
+namespace {
+int fwd_common(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
+               const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
+               float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+               void* stream, const ffa_options* options, const PagedKV& pg) {
   int rc = check_shape(shape, n_ranges);
   if (rc != FFA_OK) return rc;
   rc = check_options(options);
@@ -208,11 +247,15 @@ int ffa_fwd_ex(const ffa_shape* shape, const void* q, const void* k, const void*
   a.out = out;
   a.lse = lse;
   a.alibi = options != nullptr ? options->alibi_slopes : nullptr;
+  a.page_table = pg.page_table;
+  a.page_size = pg.page_size;
+  a.n_pages = pg.n_pages;
   a.plan = pv;
   a.status = status;
   a.wait_limit_ns = wait_limit_ns();
   return cuda_status(launch_fwd(a, s));
 }
+}  // namespace
 
 int ffa_bwd(const ffa_shape* shape, const void* q, const void* k, const void* v, const void* out,
             const float* lse, const void* dout, const int32_t* q_ranges, const int32_t* k_ranges,

@@ -70,6 +70,8 @@ struct FwdParams {
   __nv_bfloat16* out;
   float* lse;
   const float* alibi;  // per-query-head ALiBi slopes, or null
+  const int32_t* page_table;  // paged K/V: physical page of each logical page, else null
+  int page_size, n_lpages, n_pages;
   int* status;
   uint64_t wait_limit_ns;
 };
@@ -515,15 +517,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           mbar_arrive_expect_tx(&k_full[st], SM::kTileBytes);
-#pragma unroll
-          for (int b = 0; b < D / 64; ++b)
-            tma_load_2d(sm + SM::kK + st * SM::kTileBytes + b * SM::kBoxBytes, &tmK, &k_full[st],
-                        it.kvh * D + 64 * b, kt * kTile);
           mbar_arrive_expect_tx(&v_full[st], SM::kTileBytes);
+          if (p.page_table == nullptr) {
 #pragma unroll
-          for (int b = 0; b < D / 64; ++b)
-            tma_load_2d(sm + SM::kV + st * SM::kTileBytes + b * SM::kBoxBytes, &tmV, &v_full[st],
-                        it.kvh * D + 64 * b, kt * kTile);
+            for (int b = 0; b < D / 64; ++b)
+              tma_load_2d(sm + SM::kK + st * SM::kTileBytes + b * SM::kBoxBytes, &tmK, &k_full[st],
+                          it.kvh * D + 64 * b, kt * kTile);
+#pragma unroll
+            for (int b = 0; b < D / 64; ++b)
+              tma_load_2d(sm + SM::kV + st * SM::kTileBytes + b * SM::kBoxBytes, &tmV, &v_full[st],
+                          it.kvh * D + 64 * b, kt * kTile);
+          } else {
+            // Paged K/V (FlexAttention paper, section 5, Paged Attention): the tile's 128
+            // logical keys are 128 / page_size pages, each fetched from its physical page into
+            // its rows of the tile (row offsets are multiples of 8, so the 128-byte swizzle
+            // pattern is the one a whole-tile load gives).  Logical pages past the table,
+            // and table entries outside the pool (reported), load zeros: the box starts past
+            // the last physical row.
+            const int per = kTile / p.page_size;
+            for (int pj = 0; pj < per; ++pj) {
+              const int lp = kt * per + pj;
+              int y = p.n_pages * p.page_size;
+              if (lp < p.n_lpages) {
+                const int phys = p.page_table[lp];
+                if (phys >= 0 && phys < p.n_pages) {
+                  y = phys * p.page_size;
+                } else if (p.status != nullptr) {
+                  atomicOr(p.status, FFA_STATUS_BAD_PAGE);
+                }
+              }
+              const uint32_t roff = static_cast<uint32_t>(pj * p.page_size) * 128u;
+#pragma unroll
+              for (int b = 0; b < D / 64; ++b) {
+                tma_load_2d(sm + SM::kK + st * SM::kTileBytes + b * SM::kBoxBytes + roff, &tmK, &k_full[st],
+                            it.kvh * D + 64 * b, y);
+                tma_load_2d(sm + SM::kV + st * SM::kTileBytes + b * SM::kBoxBytes + roff, &tmV, &v_full[st],
+                            it.kvh * D + 64 * b, y);
+              }
+            }
+          }
           last_use[st] = static_cast<int>(u);
           ++gk;
         }
@@ -694,9 +726,13 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   }
   CUtensorMap mq, mk, mv;
   const auto& P = a.P;
+  // paged: K/V maps cover the physical pool, one page of rows per box
+  const bool paged = a.page_table != nullptr;
+  const uint64_t kv_rows = paged ? static_cast<uint64_t>(a.n_pages) * a.page_size : static_cast<uint64_t>(P.nk);
+  const uint32_t kv_box = paged ? static_cast<uint32_t>(a.page_size) : static_cast<uint32_t>(kTile);
   if (!encode_tile_map(&mq, a.q, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile) ||
-      !encode_tile_map(&mk, a.k, static_cast<uint64_t>(P.hkv) * D, P.nk, 64, kTile) ||
-      !encode_tile_map(&mv, a.v, static_cast<uint64_t>(P.hkv) * D, P.nk, 64, kTile))
+      !encode_tile_map(&mk, a.k, static_cast<uint64_t>(P.hkv) * D, kv_rows, 64, kv_box) ||
+      !encode_tile_map(&mv, a.v, static_cast<uint64_t>(P.hkv) * D, kv_rows, 64, kv_box))
     return cudaErrorInvalidValue;
   FwdParams p;
   p.nq = P.nq; p.nk = P.nk; p.hq = P.hq; p.hkv = P.hkv; p.G = P.hq / P.hkv;
@@ -709,6 +745,10 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.alibi = a.alibi;
+  p.page_table = a.page_table;
+  p.page_size = paged ? a.page_size : 0;
+  p.n_pages = paged ? static_cast<int>(a.n_pages) : 0;
+  p.n_lpages = paged ? static_cast<int>((static_cast<int64_t>(P.nk) + a.page_size - 1) / a.page_size) : 0;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
   const int grid = a.n_items < num_sms() ? a.n_items : num_sms();

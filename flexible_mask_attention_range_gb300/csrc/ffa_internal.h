@@ -185,6 +185,11 @@ struct FwdArgs {
   void* out;
   float* lse;
   const float* alibi = nullptr;  // per-query-head ALiBi slopes (device) or null
+  // Paged K/V (page_size > 0): k and v are physical page pools [n_pages * page_size, Hkv, d];
+  // logical page j of the key sequence lives in physical page page_table[j].
+  const int32_t* page_table = nullptr;
+  int page_size = 0;
+  int64_t n_pages = 0;
   PlanView plan;
   int32_t* status;
   uint64_t wait_limit_ns;

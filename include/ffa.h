@@ -59,6 +59,7 @@ extern "C" {
 #define FFA_STATUS_BAD_RANGE 1 /* a malformed slice was dropped                       */
 #define FFA_STATUS_TIMEOUT 2   /* a bounded wait inside a kernel ran out              */
 #define FFA_STATUS_SMEM 4      /* shared memory could not be aligned for the tiles    */
+#define FFA_STATUS_BAD_PAGE 8  /* a page-table entry pointed outside the page pool    */
 
 /* slice types (attn_type_map values) */
 #define FFA_FULL 0
@@ -167,6 +168,29 @@ int ffa_bwd_ex(const ffa_shape* shape, const void* q, const void* k, const void*
                const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale, float softcap, void* dq,
                void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* status, void* stream,
                const ffa_options* options);
+
+/*
+ * Forward pass over a paged key/value cache (FlexAttention paper, section 5, Paged
+ * Attention: a shared physical cache indexed through a page table, with masks written in
+ * logical positions).  Slices, masks, ALiBi and all results use logical key positions
+ * 0 .. shape->total_k - 1 exactly as ffa_fwd does; only where a key's data lives differs.
+ *   k_pages, v_pages  device bf16 [n_pages, page_size, Hkv, d], 16-byte aligned: the pool
+ *   page_table        device int32 [ceil(total_k / page_size)]: logical page j of the key
+ *                     sequence (keys j*page_size .. j*page_size + page_size - 1) is
+ *                     physical page page_table[j].  Pages may be shared or unused.
+ *   page_size         16, 32, 64 or 128 keys
+ *   n_pages           pages in the pool, >= 1, n_pages * page_size < 2^31
+ *   options           as for ffa_fwd_ex (deterministic has no effect on a forward pass)
+ * Other arguments, the workspace size and the results are those of ffa_fwd (same
+ * ffa_fwd_workspace_size()).  An entry outside [0, n_pages) makes its keys read as zeros
+ * and ORs FFA_STATUS_BAD_PAGE into *status.  Forward only: gradients through a paged cache
+ * are not provided.
+ */
+int ffa_fwd_paged(const ffa_shape* shape, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* page_table, int32_t page_size, int64_t n_pages, const int32_t* q_ranges,
+                  const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
+                  float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+                  void* stream, const ffa_options* options);
 
 /*
  * The planner alone: classify every tile of the global 128 x 128 tile grid as

@@ -5,7 +5,7 @@ anything from here; the product path never does.  See ``ffa_oracle`` for what it
 and which passages it follows.
 """
 from .ffa_oracle import (  # noqa: F401
-    CAUSAL, FULL, TILE_EMPTY, TILE_FULL, TILE_PARTIAL, backward, dense_mask, forward,
+    CAUSAL, FULL, TILE_EMPTY, TILE_FULL, TILE_PARTIAL, backward, dense_mask, forward, gather_pages,
     key_intervals, lse_merge, mask_block, normalize_slices, resolve_scale, row_intervals,
     tile_classes, visible_pairs,
 )

@@ -28,6 +28,12 @@ each row's whole key set):
     positions (the distance between two tokens of one document equals their in-document
     distance).
 
+  * Paged key/value cache -- same paper, section 5 (Paged Attention): the keys of a
+    sequence live in a shared physical cache, reached through a page table; masks and score
+    modifications keep seeing logical positions.  Logical key j is row j % page_size of
+    physical page page_table[j // page_size] (``gather_pages``); attention is then the plain
+    definition over the gathered logical keys.
+
 Readings where the pages are silent (each is listed in the design notes):
   * CAUSAL alignment inside a slice with unequal q and k lengths: bottom-right.  Pair (i, j)
     of slice [qs,qe) x [ks,ke) is visible iff qs <= i < qe, ks <= j < ke and
@@ -381,6 +387,18 @@ def backward(q, k, v, dout, q_ranges, k_ranges, attn_type_map, softmax_scale=Non
                     dk[dst, kh] += gk[sel]
                     dv[dst, kh] += gv[sel]
     return dq, dk, dv
+
+
+def gather_pages(pool, page_table, page_size: int, total_k: int) -> np.ndarray:
+    """Logical keys (or values) [total_k, ...] of a paged cache: logical key j is row
+    j % page_size of physical page page_table[j // page_size] of ``pool``
+    [n_pages, page_size, ...] (Flex Attention paper, section 5, Paged Attention)."""
+    pool = np.asarray(pool)
+    table = np.asarray(page_table, dtype=np.int64).reshape(-1)
+    out = np.empty((total_k,) + pool.shape[2:], dtype=pool.dtype)
+    for j in range(total_k):
+        out[j] = pool[table[j // page_size], j % page_size]
+    return out
 
 
 def lse_merge(outs: Iterable[np.ndarray], lses: Iterable[np.ndarray]):

@@ -77,3 +77,20 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ffa, "_LIB", None)
     with pytest.raises(ffa.FfaError):
         ffa.lib()
+
+
+def test_paged_forward_argument_checks(lib_path):
+    L = ffa.lib()
+    p = ctypes.c_void_p(16)
+    s = ffa.FfaShape(256, 256, 2, 1, 64)
+
+    def call(page_size=32, n_pages=8, table=p, shape=s):
+        return L.ffa_fwd_paged(ctypes.byref(shape), p, p, p, table, page_size, n_pages, p, p, p, 1, -1.0, 0.0, p, p,
+                               None, 0, None, None, None)
+
+    for bad in (0, 8, 48, 256):
+        assert call(page_size=bad) == 1                 # page sizes 16, 32, 64, 128 only
+    assert call(n_pages=0) == 1
+    assert call(page_size=128, n_pages=1 << 24) == 1    # pool rows must stay below 2^31
+    assert call(table=None) == 1                        # keys present, no page table
+    assert call() == 4                                  # valid paging arguments: then no workspace

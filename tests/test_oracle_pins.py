@@ -421,3 +421,36 @@ def test_alibi_zero_slopes_is_identity_and_gradients_match_finite_differences():
             x[idx] = old
             num[idx] = (fp - fm) / (2 * eps)
         assert np.abs(num - g).max() / max(1e-12, np.abs(g).max()) < 1e-6
+
+
+def test_gather_pages_hand_example():
+    # pool of 3 physical pages of 2 keys (one head, d = 1) holding 10*page + row; logical
+    # pages (2, 0) give keys 20, 21, 0, 1 -- and a 3-key sequence stops after 20, 21, 0
+    pool = np.array([[[[0.0]], [[1.0]]], [[[10.0]], [[11.0]]], [[[20.0]], [[21.0]]]])
+    got = O.gather_pages(pool, [2, 0], 2, 4)
+    assert got.reshape(-1).tolist() == [20.0, 21.0, 0.0, 1.0]
+    got3 = O.gather_pages(pool, [2, 0], 2, 3)
+    assert got3.reshape(-1).tolist() == [20.0, 21.0, 0.0]
+
+
+def test_attention_over_scattered_pages_equals_logical_attention():
+    # scatter logical K/V into a permuted pool with spare pages; attention over the gathered
+    # keys must be the attention over the logical keys (SDPA in float64 as the reference)
+    nq, nk, hq, hkv, d, ps = 24, 37, 4, 2, 8, 8
+    q, k, v = _rand((nq, hq, d), 41), _rand((nk, hkv, d), 42), _rand((nk, hkv, d), 43)
+    n_lp = -(-nk // ps)
+    rng = np.random.default_rng(44)
+    n_pages = n_lp + 3
+    table = rng.permutation(n_pages)[:n_lp]
+    kp = _rand((n_pages, ps, hkv, d), 45)
+    vp = _rand((n_pages, ps, hkv, d), 46)
+    for j in range(n_lp):
+        rows = min(ps, nk - j * ps)
+        kp[table[j], :rows] = k[j * ps:j * ps + rows]
+        vp[table[j], :rows] = v[j * ps:j * ps + rows]
+    kg, vg = O.gather_pages(kp, table, ps, nk), O.gather_pages(vp, table, ps, nk)
+    assert np.array_equal(kg, k) and np.array_equal(vg, v)
+    o, lse = O.forward(q, kg, vg, [[0, nq]], [[0, nk]], [O.FULL])
+    o_ref, lse_ref = _sdpa(q, k, v, scale=1.0 / math.sqrt(d))
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-12)

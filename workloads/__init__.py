@@ -204,3 +204,10 @@ def random_slices(total_q: int, total_k: int, n: int, seed: int, p_dummy: float 
         qr.append((qs, qe)); kr.append((ks, ke))
         ty.append(CAUSAL if float(torch.rand((), generator=g).item()) < p_causal else FULL)
     return qr, kr, ty
+
+
+def random_page_table(n_logical: int, n_pages: int, seed: int) -> torch.Tensor:
+    """Distinct physical pages for n_logical logical pages out of a pool of n_pages (a seeded
+    random permutation prefix), int32 -- the page table of a paged key/value cache."""
+    g = make_generator(seed)
+    return torch.randperm(n_pages, generator=g)[:n_logical].to(torch.int32)
