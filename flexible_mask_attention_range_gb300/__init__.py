@@ -69,6 +69,9 @@ SIGNATURES = {
                                       _P]),
     "ffa_fwd_paged": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _I32, ctypes.c_int64, _P, _P, _P,
                                      _I32, _F, _F, _P, _P, _P, _SZ, _P, _P, ctypes.POINTER(FfaOptions)]),
+    "ffa_fwd_decode_workspace_size": (_SZ, [ctypes.POINTER(FfaShape), _I32, _I32]),
+    "ffa_fwd_decode": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _I32, ctypes.c_int64, _P, _P, _P,
+                                      _I32, _I32, _F, _F, _P, _P, _P, _SZ, _P, _P, ctypes.POINTER(FfaOptions)]),
     "ffa_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(FfaShape), _P, _P, _P, _P, _P, _P, _I32, _F, _F, _P, _P,
                                        _P, _P]),
     "ffa_set_kernel_events": (ctypes.c_int, [_P, _P, _P, _P]),
@@ -248,6 +251,55 @@ def ffa_fwd_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
                              _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev),
                              ctypes.byref(opts) if opts is not None else None)
     _check(rc, "ffa_fwd_paged")
+    return out, lse
+
+
+def ffa_fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_ranges, attn_type_map,
+                   max_seqlen_q: int, softmax_scale: Optional[float] = None, softcap: float = 0.0,
+                   page_table: Optional[torch.Tensor] = None, total_k: Optional[int] = None,
+                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Decoding form of ffa_fwd (see include/ffa.h): the query heads of a key/value head are
+    processed as rows of one problem.  Dense cache: k, v [Nk, Hkv, d].  Paged cache: k, v are
+    [n_pages, page_size, Hkv, d] pools, ``page_table`` int32 and ``total_k`` the logical key
+    count.  ``max_seqlen_q`` bounds the query tokens of any CAUSAL slice."""
+    dev = q.device
+    nq, hq, d = q.shape
+    _need(q, "q", torch.bfloat16, dev)
+    if page_table is None:
+        nk, hkv = k.shape[0], k.shape[1]
+        _need(k, "k", torch.bfloat16, dev, (nk, hkv, d))
+        _need(v, "v", torch.bfloat16, dev, (nk, hkv, d))
+        page_size, n_pages = 0, 0
+    else:
+        n_pages, page_size, hkv = k.shape[0], k.shape[1], k.shape[2]
+        _need(k, "k", torch.bfloat16, dev, (n_pages, page_size, hkv, d))
+        _need(v, "v", torch.bfloat16, dev, (n_pages, page_size, hkv, d))
+        if total_k is None:
+            raise ValueError("total_k is required with a page table")
+        nk = int(total_k)
+        _need(page_table, "page_table", torch.int32, dev, ((nk + page_size - 1) // page_size,))
+    qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
+    if out is None:
+        out = torch.empty(nq, hq, d, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(hq, nq, dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev, (nq, hq, d))
+    _need(lse, "lse", torch.float32, dev, (hq, nq))
+    R = qr.shape[0]
+    shp = _shape(nq, nk, hq, hkv, d)
+    ws_bytes = int(lib().ffa_fwd_decode_workspace_size(ctypes.byref(shp), R, int(max_seqlen_q)))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    if status is not None:
+        _need(status, "status", torch.int32, dev)
+    scale = -1.0 if softmax_scale is None else float(softmax_scale)
+    rc = lib().ffa_fwd_decode(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(page_table), int(page_size),
+                              int(n_pages), _ptr(qr), _ptr(kr), _ptr(ty), R, int(max_seqlen_q), scale,
+                              float(softcap), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                              _ptr(status), _stream(dev), None)
+    _check(rc, "ffa_fwd_decode")
     return out, lse
 
 

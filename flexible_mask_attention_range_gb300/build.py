@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libffa.so")
-SOURCES = ["ffa_api.cu", "ffa_plan.cu", "ffa_fwd.cu", "ffa_bwd.cu", "ffa_noalloc.cu"]
+SOURCES = ["ffa_api.cu", "ffa_plan.cu", "ffa_fwd.cu", "ffa_bwd.cu", "ffa_noalloc.cu", "ffa_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,218 @@
+// ffa_fwd_decode: attention for a few new query tokens per sequence (decoding) with GQA
+// head packing, over a dense or paged key/value cache.
+//
+// A decoding step has one (or a few) query tokens per sequence and a long key sequence.
+// The FlexAttention paper (section 4, template-based lowering) has a separate decoding
+// template with grouped-query attention support, compared against FlashDecoding in section
+// 6; it does not spell out that template.  On the token-major layout the forward kernel's
+// 128-row query tiles would mix many sequences and read every key tile once per pair of
+// query heads, so this library's decoding path packs P query heads of each token into P
+// consecutive rows of a problem with Hq / P heads:
+//     packed row (i * P + g), packed head h  <-  token i, query head h * P + g,
+// with P = G / 2 when G = Hq / Hkv is even (two packed heads per key/value head: they form
+// a head pair of the forward kernel and share every K/V tile it loads) and P = G otherwise.
+// A packed query tile then holds 128 / P tokens, and every key tile is read once per
+// (query tile, key/value head).  Long key sequences with few query tiles are split across
+// CTAs and merged by LSE, as in the plain forward pass.
+//
+// Slices are rewritten for the packed rows: a FULL slice [qs, qe) x [ks, ke) becomes
+// [qs * P, qe * P) x [ks, ke); a CAUSAL slice with m = qe - qs query tokens becomes m FULL
+// slices, one per token i, over the keys that token sees under the bottom-right alignment
+// used everywhere in this library (j <= i + ke - qe).  max_seqlen_q bounds m, so the
+// rewritten list has a fixed length n_ranges * max_seqlen_q (unused entries are empty
+// slices).  Packing, rewriting and unpacking are three small kernels around ffa_fwd_ex /
+// ffa_fwd_paged.
+#include <cstdint>
+
+#include "../../include/ffa.h"
+#include "ffa_internal.h"
+
+namespace ffa {
+namespace {
+
+// q [N, Hq, d] -> qp [N * P, Hq / P, d], in 16-byte units (d / 8 of them per row).
+__global__ void __launch_bounds__(256) decode_pack_q(const uint4* __restrict__ q, uint4* __restrict__ qp,
+                                                     int64_t n, int hq, int P, int d) {
+  const int hp = hq / P;
+  const int64_t per_row = d / 8;
+  const int64_t total = n * hq * per_row;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = idx / per_row, c = idx - row * per_row;  // packed row = (i * P + g) * hp + h
+    const int64_t h = row % hp, ig = row / hp;
+    const int64_t g = ig % P, i = ig / P;
+    qp[idx] = q[(i * hq + h * P + g) * per_row + c];
+  }
+}
+
+// op [N * P, Hq / P, d] -> out [N, Hq, d]; lsep [Hq / P, N * P] -> lse [Hq, N].
+__global__ void __launch_bounds__(256) decode_unpack(const uint4* __restrict__ op, uint4* __restrict__ out,
+                                                     const float* __restrict__ lsep, float* __restrict__ lse,
+                                                     int64_t n, int hq, int P, int d) {
+  const int hp = hq / P;
+  const int64_t per_row = d / 8;
+  const int64_t total = n * hq * per_row;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total; idx += stride) {
+    const int64_t row = idx / per_row, c = idx - row * per_row;  // out row = i * hq + head
+    const int64_t head = row % hq, i = row / hq;
+    const int64_t h = head / P, g = head - h * P;
+    out[idx] = op[((i * P + g) * hp + h) * per_row + c];
+  }
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n * hq; idx += stride) {
+    const int64_t head = idx / n, i = idx - head * n;
+    const int64_t h = head / P, g = head - h * P;
+    lse[idx] = lsep[h * (n * P) + i * P + g];
+  }
+}
+
+// Slice s, token slot u -> rewritten slice s * M + u (see the file comment).  Invalid slices
+// (bounds, type, or a CAUSAL slice longer than M) are reported with FFA_STATUS_BAD_RANGE and
+// dropped, as the planner does for the plain forward pass.
+__global__ void __launch_bounds__(256) decode_slices(const int32_t* __restrict__ qr, const int32_t* __restrict__ kr,
+                                                     const int32_t* __restrict__ ty, int R, int M, int P, int64_t nq,
+                                                     int64_t nk, int32_t* __restrict__ qr2, int32_t* __restrict__ kr2,
+                                                     int32_t* __restrict__ ty2, int32_t* status) {
+  const int64_t total = static_cast<int64_t>(R) * M;
+  for (int64_t slot = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; slot < total;
+       slot += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t s = slot / M;
+    const int u = static_cast<int>(slot - s * M);
+    const int64_t qs = qr[2 * s], qe = qr[2 * s + 1], ks = kr[2 * s], ke = kr[2 * s + 1];
+    const int t = ty[s];
+    int64_t a = 0, b = 0, c = 0, e = 0;  // empty slice unless set below
+    const bool valid = qs >= 0 && qs <= qe && qe <= nq && ks >= 0 && ks <= ke && ke <= nk && (t == FFA_FULL || t == FFA_CAUSAL);
+    const int64_t m = qe - qs;
+    if (!valid || (t == FFA_CAUSAL && m > M)) {
+      if (u == 0 && status != nullptr) atomicOr(status, FFA_STATUS_BAD_RANGE);
+    } else if (t == FFA_FULL) {
+      if (u == 0) {
+        a = qs * P; b = qe * P; c = ks; e = ke;
+      }
+    } else if (u < m) {
+      const int64_t i = qs + u;
+      const int64_t hi = ke - m + 1 + u < ke ? ke - m + 1 + u : ke;  // keys j < hi, i.e. j <= i + ke - qe
+      if (hi > ks) {
+        a = i * P; b = (i + 1) * P; c = ks; e = hi;
+      }
+    }
+    qr2[2 * slot] = static_cast<int32_t>(a);
+    qr2[2 * slot + 1] = static_cast<int32_t>(b);
+    kr2[2 * slot] = static_cast<int32_t>(c);
+    kr2[2 * slot + 1] = static_cast<int32_t>(e);
+    ty2[slot] = FFA_FULL;
+  }
+}
+
+// Query heads per packed row group: G / 2 for even G (packed heads form head pairs), else G.
+int pack_factor(int G) { return (G % 2 == 0) ? G / 2 : G; }
+
+struct DecodeLayout {
+  size_t qp = 0, op = 0, lsep = 0, qr2 = 0, kr2 = 0, ty2 = 0, inner = 0, total = 0;
+  int64_t R2 = 0;
+  int P = 1;
+  ffa_shape inner_shape{};
+};
+
+bool decode_layout(const ffa_shape* s, int32_t n_ranges, int32_t max_seqlen_q, DecodeLayout* L) {
+  if (s == nullptr || n_ranges < 0 || max_seqlen_q < 1 || s->num_heads_kv < 1 || s->num_heads_q < 1 ||
+      s->num_heads_q % s->num_heads_kv != 0 || s->total_q < 0)
+    return false;
+  const int P = pack_factor(s->num_heads_q / s->num_heads_kv);
+  const int64_t R2 = static_cast<int64_t>(n_ranges) * max_seqlen_q;
+  if (R2 > (static_cast<int64_t>(1) << 30)) return false;
+  L->R2 = R2;
+  L->P = P;
+  L->inner_shape.total_q = s->total_q * P;
+  L->inner_shape.total_k = s->total_k;
+  L->inner_shape.num_heads_q = s->num_heads_q / P;
+  L->inner_shape.num_heads_kv = s->num_heads_kv;
+  L->inner_shape.head_dim = s->head_dim;
+  const size_t inner = ffa_fwd_workspace_size(&L->inner_shape, static_cast<int32_t>(R2));
+  if (inner == 0) return false;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+  const size_t rows = static_cast<size_t>(s->total_q) * s->num_heads_q;
+  L->qp = take(rows * s->head_dim * 2);
+  L->op = take(rows * s->head_dim * 2);
+  L->lsep = take(rows * 4);
+  L->qr2 = take(static_cast<size_t>(R2) * 8);
+  L->kr2 = take(static_cast<size_t>(R2) * 8);
+  L->ty2 = take(static_cast<size_t>(R2) * 4);
+  L->inner = take(inner);
+  L->total = o;
+  return true;
+}
+
+}  // namespace
+}  // namespace ffa
+
+using namespace ffa;
+
+extern "C" {
+
+size_t ffa_fwd_decode_workspace_size(const ffa_shape* shape, int32_t n_ranges, int32_t max_seqlen_q) {
+  DecodeLayout L;
+  if (!decode_layout(shape, n_ranges, max_seqlen_q, &L)) return 0;
+  return L.total;
+}
+
+int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* page_table,
+                   int32_t page_size, int64_t n_pages, const int32_t* q_ranges, const int32_t* k_ranges,
+                   const int32_t* attn_type_map, int32_t n_ranges, int32_t max_seqlen_q, float softmax_scale,
+                   float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+                   void* stream, const ffa_options* options) {
+  if (shape == nullptr || n_ranges < 0 || max_seqlen_q < 1) return FFA_ERR_INVALID_ARG;
+  if (options != nullptr && options->alibi_slopes != nullptr) return FFA_ERR_UNSUPPORTED;
+  if (shape->head_dim != 64 && shape->head_dim != 128) return FFA_ERR_UNSUPPORTED;
+  if (shape->num_heads_kv < 1 || shape->num_heads_q < 1 || shape->num_heads_q % shape->num_heads_kv != 0)
+    return FFA_ERR_INVALID_ARG;
+  const int P = pack_factor(shape->num_heads_q / shape->num_heads_kv);
+  if (shape->total_q < 0 || shape->total_q * P > FFA_MAX_TOKENS) return FFA_ERR_UNSUPPORTED;
+  DecodeLayout L;
+  if (!decode_layout(shape, n_ranges, max_seqlen_q, &L)) return FFA_ERR_INVALID_ARG;
+  const int64_t nq = shape->total_q;
+  if (nq > 0 && (q == nullptr || out == nullptr || lse == nullptr)) return FFA_ERR_INVALID_ARG;
+  if (n_ranges > 0 && (q_ranges == nullptr || k_ranges == nullptr || attn_type_map == nullptr))
+    return FFA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FFA_ERR_INVALID_ARG;
+  if (nq == 0) return FFA_OK;
+  if (workspace == nullptr || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FFA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* wb = static_cast<char*>(workspace);
+  const int hq = shape->num_heads_q, d = shape->head_dim;
+  const int nsm = num_sms();
+  const int64_t units = nq * hq * (d / 8);
+  const int blocks = static_cast<int>(units / 256 + 1 < static_cast<int64_t>(nsm) * 8 ? units / 256 + 1 : nsm * 8);
+  decode_pack_q<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(q), reinterpret_cast<uint4*>(wb + L.qp), nq, hq, P, d);
+  if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+  int32_t* qr2 = reinterpret_cast<int32_t*>(wb + L.qr2);
+  int32_t* kr2 = reinterpret_cast<int32_t*>(wb + L.kr2);
+  int32_t* ty2 = reinterpret_cast<int32_t*>(wb + L.ty2);
+  if (L.R2 > 0) {
+    const int sb = static_cast<int>(L.R2 / 256 + 1 < static_cast<int64_t>(nsm) * 4 ? L.R2 / 256 + 1 : nsm * 4);
+    decode_slices<<<sb, 256, 0, s>>>(q_ranges, k_ranges, attn_type_map, n_ranges, max_seqlen_q, P, nq,
+                                     shape->total_k, qr2, kr2, ty2, status);
+    if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+  }
+  const size_t inner_bytes = workspace_bytes - L.inner;
+  int rc;
+  if (page_table == nullptr) {
+    rc = ffa_fwd_ex(&L.inner_shape, wb + L.qp, k, v, qr2, kr2, ty2, static_cast<int32_t>(L.R2), softmax_scale, softcap,
+                    wb + L.op, reinterpret_cast<float*>(wb + L.lsep), wb + L.inner, inner_bytes, status, stream,
+                    options);
+  } else {
+    rc = ffa_fwd_paged(&L.inner_shape, wb + L.qp, k, v, page_table, page_size, n_pages, qr2, kr2, ty2,
+                       static_cast<int32_t>(L.R2), softmax_scale, softcap, wb + L.op,
+                       reinterpret_cast<float*>(wb + L.lsep), wb + L.inner, inner_bytes, status, stream, options);
+  }
+  if (rc != FFA_OK) return rc;
+  decode_unpack<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(wb + L.op), static_cast<uint4*>(out),
+                                       reinterpret_cast<const float*>(wb + L.lsep), lse, nq, hq, P, d);
+  return cudaGetLastError() == cudaSuccess ? FFA_OK : FFA_ERR_CUDA;
+}
+
+}  // extern "C"

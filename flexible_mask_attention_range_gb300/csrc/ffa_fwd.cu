@@ -655,14 +655,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 // LSE merge of split rows: for a group whose work list was cut into chunks, every row combines
 // its chunks' partial results, L = log sum_c e^{L_c} and O = sum_c e^{L_c - L} O_c (the
 // chunks cover disjoint key sets of the row); rows whose chunks all have L_c = -inf get
-// O = 0 and L = -inf.  One CTA per (group, head slot), one thread per row of either tile.
+// O = 0 and L = -inf.  One CTA per (group, head slot, sub-tile, 32-row block, 32-column
+// block); thread = (row, 4 columns), so a warp reads whole 128-byte lines of 4 rows.
+constexpr int kMergeRows = 32;
 template <int D>
 __global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
-  const int g = blockIdx.x / p.slots, slot = blockIdx.x - (blockIdx.x / p.slots) * p.slots;
+  constexpr int kColBlocks = D / 32;
+  int b = blockIdx.x;
+  const int cb = b % kColBlocks;
+  b /= kColBlocks;
+  const int rb = b % (kTile / kMergeRows);
+  b /= kTile / kMergeRows;
+  const int sub = b & 1;
+  b >>= 1;
+  const int g = b / p.slots, slot = b - (b / p.slots) * p.slots;
   const int nch = p.plan.grp_nch[g];
   if (nch <= 1) return;
   const int ps = p.plan.grp_pslot[g];
-  const int sub = threadIdx.x >> 7, r = threadIdx.x & 127;
+  const int r = rb * kMergeRows + (threadIdx.x >> 3), c4 = (threadIdx.x & 7) * 4 + cb * 32;
   int qt, h;
   if (p.head_pair) {
     qt = g;
@@ -676,42 +686,28 @@ __global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
   auto prow = [&](int c) { return (static_cast<size_t>(ps + c) * p.slots + slot) * 2 * kTile + sub * kTile + r; };
   float mx = -INFINITY;
   for (int c = 0; c < nch; ++c) mx = fmaxf(mx, p.plan.part_lse[prow(c)]);
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
+  uint2* dst = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D + c4);
+  const bool lse_writer = (cb == 0) && ((threadIdx.x & 7) == 0);
   if (mx == -INFINITY) {
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-    p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
+    *dst = make_uint2(0u, 0u);
+    if (lse_writer) p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
     return;
   }
-  float acc[D];
-#pragma unroll
-  for (int k = 0; k < D; ++k) acc[k] = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   float wsum = 0.0f;
   for (int c = 0; c < nch; ++c) {
     const size_t pr = prow(c);
     const float w = ex2_approx((p.plan.part_lse[pr] - mx) * kLog2e);
     wsum += w;
-    const float4* src = reinterpret_cast<const float4*>(p.plan.part_o + pr * D);
-#pragma unroll
-    for (int k = 0; k < D / 4; ++k) {
-      const float4 v = src[k];
-      acc[4 * k] = fmaf(w, v.x, acc[4 * k]);
-      acc[4 * k + 1] = fmaf(w, v.y, acc[4 * k + 1]);
-      acc[4 * k + 2] = fmaf(w, v.z, acc[4 * k + 2]);
-      acc[4 * k + 3] = fmaf(w, v.w, acc[4 * k + 3]);
-    }
+    const float4 v = *reinterpret_cast<const float4*>(p.plan.part_o + pr * D + c4);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
   }
   const float inv = 1.0f / wsum;
-#pragma unroll
-  for (int k = 0; k < D / 8; ++k) {
-    uint4 v;
-    v.x = pack_bf16x2(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
-    v.y = pack_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
-    v.z = pack_bf16x2(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
-    v.w = pack_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
-    dst[k] = v;
-  }
-  p.lse[static_cast<size_t>(h) * p.nq + row] = mx + lg2_approx(wsum) * kLn2;
+  *dst = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (lse_writer) p.lse[static_cast<size_t>(h) * p.nq + row] = mx + lg2_approx(wsum) * kLn2;
 }
 
 template <int D, bool kCap, bool kBias>
@@ -758,7 +754,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   if (g_kernel_events.fwd_stop != nullptr) cudaEventRecord(g_kernel_events.fwd_stop, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !a.split) return e;
-  ffa_fwd_merge<D><<<a.ngrp * a.slots, 256, 0, stream>>>(p);
+  ffa_fwd_merge<D><<<a.ngrp * a.slots * 2 * (kTile / kMergeRows) * (D / 32), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

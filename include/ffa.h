@@ -193,6 +193,26 @@ int ffa_fwd_paged(const ffa_shape* shape, const void* q, const void* k_pages, co
                   void* stream, const ffa_options* options);
 
 /*
+ * Decoding: few new query tokens per sequence against long (optionally paged) key caches
+ * (FlexAttention paper: a decoding template with grouped-query attention support, section
+ * 4; decoding measured against FlashDecoding, section 6).  Same arguments and results as
+ * ffa_fwd (page_table == NULL) or ffa_fwd_paged (page_table != NULL), plus
+ *   max_seqlen_q  >= 1: the most query tokens any CAUSAL slice has (the max_seqlen_q
+ *                 argument of flex_flash_attn_func); a CAUSAL slice with more is dropped and
+ *                 reported with FFA_STATUS_BAD_RANGE
+ * The query heads of every token are processed as rows of the key/value head they share
+ * (G / 2 rows per packed head when G = Hq / Hkv is even, G otherwise), so each key tile is
+ * read once per key/value head instead of once per pair of query heads.  ALiBi is not available here (FFA_ERR_UNSUPPORTED).  Requires
+ * total_q * G <= FFA_MAX_TOKENS.  workspace: ffa_fwd_decode_workspace_size() bytes.
+ */
+size_t ffa_fwd_decode_workspace_size(const ffa_shape* shape, int32_t n_ranges, int32_t max_seqlen_q);
+int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* page_table,
+                   int32_t page_size, int64_t n_pages, const int32_t* q_ranges, const int32_t* k_ranges,
+                   const int32_t* attn_type_map, int32_t n_ranges, int32_t max_seqlen_q, float softmax_scale,
+                   float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+                   void* stream, const ffa_options* options);
+
+/*
  * The planner alone: classify every tile of the global 128 x 128 tile grid as
  * FFA_TILE_EMPTY / PARTIAL / FULL under the union of the slices (block classification of
  * the Flex Attention paper, section 4, "Block Sparsity" / "Full Block Optimization"),

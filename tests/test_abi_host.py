@@ -94,3 +94,22 @@ def test_paged_forward_argument_checks(lib_path):
     assert call(page_size=128, n_pages=1 << 24) == 1    # pool rows must stay below 2^31
     assert call(table=None) == 1                        # keys present, no page table
     assert call() == 4                                  # valid paging arguments: then no workspace
+
+
+def test_decode_argument_checks(lib_path):
+    L = ffa.lib()
+    p = ctypes.c_void_p(16)
+    s = ffa.FfaShape(16, 4096, 8, 2, 128)
+    assert L.ffa_fwd_decode_workspace_size(ctypes.byref(s), 16, 1) > 0
+    assert L.ffa_fwd_decode_workspace_size(ctypes.byref(s), 16, 0) == 0      # max_seqlen_q >= 1
+    assert L.ffa_fwd_decode_workspace_size(ctypes.byref(ffa.FfaShape(16, 16, 6, 4, 64)), 1, 1) == 0
+
+    def call(shape=s, max_q=1, opts=None):
+        return L.ffa_fwd_decode(ctypes.byref(shape), p, p, p, None, 0, 0, p, p, p, 16, max_q, -1.0, 0.0, p, p,
+                                None, 0, None, None, opts)
+
+    assert call(max_q=0) == 1
+    assert call(shape=ffa.FfaShape(16, 4096, 8, 2, 96)) == 2                # head_dim
+    slopes = ffa.FfaOptions(16)
+    assert call(opts=ctypes.byref(slopes)) == 2                             # ALiBi not here
+    assert call() == 4                                                      # then: no workspace

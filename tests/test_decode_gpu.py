@@ -1,0 +1,109 @@
+"""Decoding (ffa_fwd_decode): a few new query tokens per sequence against long key caches,
+dense and paged, checked against ffa_fwd on the same inputs and against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+import flexible_mask_attention_range_gb300 as ffa
+from _parity import assert_lse_close, assert_out_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(lib_path):
+    yield
+
+
+def _batch(n_seq, q_len, seed, lo=100, hi=3000):
+    """Packed decode batch: sequence s has q_len new tokens at the end of kv_len[s] keys;
+    slices (q range of its tokens, k range of its keys, CAUSAL: bottom-right alignment)."""
+    g = W.make_generator(seed)
+    kv_len = (torch.randint(lo, hi, (n_seq,), generator=g)).tolist()
+    qr, kr, ty = [], [], []
+    q0 = k0 = 0
+    for L in kv_len:
+        qr.append([q0, q0 + q_len])
+        kr.append([k0, k0 + L])
+        ty.append(O.CAUSAL)
+        q0 += q_len
+        k0 += L
+    return qr, kr, ty, q0, k0
+
+
+CASES = [
+    # n_seq, q_len, hq, hkv, d, seed
+    (16, 1, 8, 1, 128, 1),
+    (40, 1, 16, 4, 128, 2),
+    (7, 3, 8, 2, 64, 3),
+    (64, 1, 4, 4, 128, 4),
+    (3, 4, 32, 4, 128, 5),
+]
+
+
+@pytest.mark.parametrize("n_seq,q_len,hq,hkv,d,seed", CASES)
+def test_decode_matches_forward_and_oracle(n_seq, q_len, hq, hkv, d, seed):
+    qr, kr, ty, nq, nk = _batch(n_seq, q_len, seed)
+    g = W.make_generator(seed + 100)
+    q = torch.randn(nq, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o_d, l_d = ffa.ffa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, max_seqlen_q=q_len, status=status)
+    o_f, l_f = ffa.ffa_fwd(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ro, rl = O.forward(q, k, v, qr, kr, ty)
+    assert_out_close(to64(o_d), ro)
+    assert_lse_close(to64(l_d), rl)
+    # same arithmetic per row as the token-major forward pass, up to summation order
+    assert (o_d.float() - o_f.float()).abs().max().item() <= 2e-2
+    assert (l_d - l_f).abs().max().item() <= 1e-3
+
+
+def test_decode_paged_cache():
+    n_seq, q_len, hq, hkv, d, page = 12, 2, 16, 2, 128, 32
+    qr, kr, ty, nq, nk = _batch(n_seq, q_len, 9, 200, 2500)
+    g = W.make_generator(109)
+    q = torch.randn(nq, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    n_lp = math.ceil(nk / page)
+    n_pages = n_lp + 5
+    table = W.random_page_table(n_lp, n_pages, 110)
+    kp = torch.zeros(n_pages, page, hkv, d, dtype=torch.bfloat16)
+    vp = torch.zeros(n_pages, page, hkv, d, dtype=torch.bfloat16)
+    for j in range(n_lp):
+        rows = min(page, nk - j * page)
+        kp[int(table[j]), :rows] = k[j * page:j * page + rows]
+        vp[int(table[j]), :rows] = v[j * page:j * page + rows]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o_p, l_p = ffa.ffa_fwd_decode(q.cuda(), kp.cuda(), vp.cuda(), qr, kr, ty, max_seqlen_q=q_len,
+                                  page_table=table.cuda(), total_k=nk, status=status)
+    o_d, l_d = ffa.ffa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, max_seqlen_q=q_len)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(o_p, o_d) and torch.equal(l_p, l_d)
+    kg = O.gather_pages(kp.float().numpy(), table.numpy(), page, nk)
+    vg = O.gather_pages(vp.float().numpy(), table.numpy(), page, nk)
+    ro, rl = O.forward(q, kg, vg, qr, kr, ty)
+    assert_out_close(to64(o_p), ro)
+    assert_lse_close(to64(l_p), rl)
+
+
+def test_decode_reports_causal_slice_longer_than_max_seqlen_q():
+    qr, kr, ty, nq, nk = _batch(4, 3, 11, 200, 400)
+    g = W.make_generator(111)
+    q = torch.randn(nq, 4, 64, generator=g).to(torch.bfloat16)
+    k = torch.randn(nk, 2, 64, generator=g).to(torch.bfloat16)
+    v = torch.randn(nk, 2, 64, generator=g).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, l = ffa.ffa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, max_seqlen_q=2, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & ffa.STATUS_BAD_RANGE
+    # every slice was dropped: every row is empty (O = 0, LSE = -inf)
+    assert torch.count_nonzero(o).item() == 0 and bool(torch.isinf(l).all())
