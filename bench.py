@@ -368,8 +368,8 @@ def oracle_sample(w: W.Workload, inputs, rows: np.ndarray):
     return dt, flops
 
 
-# about 10-20 s of float64 oracle work on the 64K workload (roughly 0.1 s per sampled row)
-CPU_BASELINE_ROWS = 128
+# about 15 s of float64 oracle work on the 64K workload on the GPU host (about 0.04 s per row)
+CPU_BASELINE_ROWS = 384
 
 
 def cpu_threads() -> int:

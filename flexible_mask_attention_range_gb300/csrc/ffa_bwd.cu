@@ -8,7 +8,7 @@
 // out.backward(do)) without fixing the kernel; this follows the usual recomputation scheme.
 //
 // Three launches after the column planner:
-//   1. ffa_bwd_pre: D_i (fp32) and LSE_i * log2(e) padded to whole tiles, dq accumulator = 0.
+//   1. ffa_bwd_pre: -D_i (fp32) and -LSE_i * log2(e) padded to whole tiles, dq accumulator = 0.
 //   2. ffa_bwd_kernel: KV-stationary.  One work item = (key tile, KV head); its CTA walks the
 //      query tiles of the key tile's column list and the G query heads of the group.  Five
 //      tcgen05 GEMMs per step: S^T = K Q^T and dP^T = V dO^T (keys on TMEM lanes), then
@@ -352,28 +352,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k4 = 0; k4 < 8; ++k4) {
             const float4 l4 = *reinterpret_cast<const float4*>(stat + c0 + 32 * c + 4 * k4);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            // the row statistics are stored negated: -LSE * log2(e) (see ffa_bwd_pre)
             float pv[4], pd[4];
+            if (kCap) {
 #pragma unroll
-            for (int h4 = 0; h4 < 4; ++h4) {
-              const int col = c0 + 32 * c + 4 * k4 + h4;
-              const float s = __uint_as_float(sv[4 * k4 + h4]);
-              // ALiBi (log2 domain): slope * log2(e) * (key j - query qt*128+col)
-              const float lb = kBias ? fmaf(-slope_log2, static_cast<float>(col), bbase) - lv[h4] : -lv[h4];
-              float pr;
-              if (kCap) {
-                const float x = capped_log2(s, p.cap_c, p.cap_k);
-                pr = ex2_approx(x + lb);
+              for (int h4 = 0; h4 < 4; ++h4) {
+                const int col = c0 + 32 * c + 4 * k4 + h4;
+                // ALiBi (log2 domain): slope * log2(e) * (key j - query qt*128+col)
+                const float lb = kBias ? fmaf(-slope_log2, static_cast<float>(col), bbase) + lv[h4] : lv[h4];
+                const float x = capped_log2(__uint_as_float(sv[4 * k4 + h4]), p.cap_c, p.cap_k);
+                float pr = ex2_approx(x + lb);
                 const float th = x * p.inv_cap_c;
                 pd[h4] = pr * (1.0f - th * th);
-              } else {
-                pr = ex2_approx(fmaf(s, p.scale_log2, lb));
-                pd[h4] = pr;
+                if (kM && mk && !((w[col >> 5] >> (col & 31)) & 1u)) {
+                  pr = 0.0f;
+                  pd[h4] = 0.0f;
+                }
+                pv[h4] = pr;
               }
-              if (kM && mk && !((w[col >> 5] >> (col & 31)) & 1u)) {
-                pr = 0.0f;
-                pd[h4] = 0.0f;
+            } else {
+              // two columns per packed fp32 pair instruction
+              const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+#pragma unroll
+              for (int hp = 0; hp < 2; ++hp) {
+                const int col0 = c0 + 32 * c + 4 * k4 + 2 * hp;
+                float2 lb2 = make_float2(lv[2 * hp], lv[2 * hp + 1]);
+                if (kBias) lb2 = make_float2(fmaf(-slope_log2, static_cast<float>(col0), bbase) + lv[2 * hp],
+                                             fmaf(-slope_log2, static_cast<float>(col0 + 1), bbase) + lv[2 * hp + 1]);
+                const float2 y = fma2(make_float2(__uint_as_float(sv[4 * k4 + 2 * hp]), __uint_as_float(sv[4 * k4 + 2 * hp + 1])), sc2, lb2);
+                float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+                if (kM && mk) {
+                  if (!((w[col0 >> 5] >> (col0 & 31)) & 1u)) p0 = 0.0f;
+                  if (!((w[(col0 + 1) >> 5] >> ((col0 + 1) & 31)) & 1u)) p1 = 0.0f;
+                }
+                pv[2 * hp] = p0;
+                pv[2 * hp + 1] = p1;
               }
-              pv[h4] = pr;
             }
             pk[2 * k4] = pack_bf16x2(pv[0], pv[1]);
             pk[2 * k4 + 1] = pack_bf16x2(pv[2], pv[3]);
@@ -416,12 +430,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k4 = 0; k4 < 8; ++k4) {
             const float4 d4 = *reinterpret_cast<const float4*>(Drow + c0 + 32 * c + 4 * k4);
             const uint32_t pa = pp[16 * c + 2 * k4], pb = pp[16 * c + 2 * k4 + 1];
-            const float d0 = __uint_as_float(pa << 16) * (__uint_as_float(dv[4 * k4]) - d4.x);
-            const float d1 = __uint_as_float(pa & 0xffff0000u) * (__uint_as_float(dv[4 * k4 + 1]) - d4.y);
-            const float d2 = __uint_as_float(pb << 16) * (__uint_as_float(dv[4 * k4 + 2]) - d4.z);
-            const float d3 = __uint_as_float(pb & 0xffff0000u) * (__uint_as_float(dv[4 * k4 + 3]) - d4.w);
-            pk[2 * k4] = pack_bf16x2(d0, d1);
-            pk[2 * k4 + 1] = pack_bf16x2(d2, d3);
+            const float2 e01 = mul2(make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xffff0000u)),
+                                    add2(make_float2(__uint_as_float(dv[4 * k4]), __uint_as_float(dv[4 * k4 + 1])),
+                                         make_float2(d4.x, d4.y)));
+            const float2 e23 = mul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)),
+                                    add2(make_float2(__uint_as_float(dv[4 * k4 + 2]), __uint_as_float(dv[4 * k4 + 3])),
+                                         make_float2(d4.z, d4.w)));
+            pk[2 * k4] = pack_bf16x2(e01.x, e01.y);
+            pk[2 * k4 + 1] = pack_bf16x2(e23.x, e23.y);
           }
           tmem_st16(tP + 16 * c, pk);
           // shared-memory copy: row r, this half's queries 32c..32c+31 -> 16-byte chunks
@@ -689,7 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// D_i = dO_i . O_i and LSE_i * log2(e) per (head, row), padded to whole tiles; zero the dq
+// -D_i = -(dO_i . O_i) and -LSE_i * log2(e) per (head, row), padded to whole tiles (stored
+// negated so the main kernel adds them with packed pair instructions); zero the dq
 // accumulator.  One warp per (row, head).
 template <int D>
 __global__ void __launch_bounds__(256) ffa_bwd_pre(const __nv_bfloat16* __restrict__ out,
@@ -704,7 +721,7 @@ __global__ void __launch_bounds__(256) ffa_bwd_pre(const __nv_bfloat16* __restri
        wi += nwarps) {
     const int h = static_cast<int>(wi / qpad);
     const int i = static_cast<int>(wi - static_cast<size_t>(h) * qpad);
-    float dsum = 0.0f, l2 = INFINITY;
+    float dsum = 0.0f, l2 = -INFINITY;
     if (i < nq) {
       const size_t base = (static_cast<size_t>(i) * hq + h) * D;
       constexpr int kPer = D / 32;  // 2 or 4 elements per lane
@@ -718,10 +735,10 @@ __global__ void __launch_bounds__(256) ffa_bwd_pre(const __nv_bfloat16* __restri
 #pragma unroll
       for (int e = 0; e < kPer; ++e) z[e] = 0.0f;
       const float l = lse[static_cast<size_t>(h) * nq + i];
-      l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+      l2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
     }
     if (lane == 0) {
-      rowD[wi] = i < nq ? dsum : 0.0f;
+      rowD[wi] = i < nq ? -dsum : 0.0f;
       lse2[wi] = l2;
     }
   }

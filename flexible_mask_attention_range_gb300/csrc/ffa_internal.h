@@ -203,8 +203,8 @@ struct BwdArgs {
   const void *q, *k, *v, *out, *dout;
   const float* lse;
   void *dq, *dk, *dv;
-  float* rowD;   // D_i = dO_i . O_i, [Hq, nqt*128], 0 beyond Nq
-  float* lse2;   // LSE_i * log2(e), [Hq, nqt*128], +inf for empty rows and beyond Nq
+  float* rowD;   // -D_i = -(dO_i . O_i), [Hq, nqt*128], 0 beyond Nq
+  float* lse2;   // -LSE_i * log2(e), [Hq, nqt*128], -inf for empty rows and beyond Nq
   float* dqacc;  // float32 [Nq, Hq, d]
   const float* alibi = nullptr;
   int deterministic = 0;
