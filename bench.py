@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -230,7 +231,8 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local: int):
             e.record()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clock_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
+    clock_dir = os.environ.get("FFA_BENCH_CLOCKS_DIR", tempfile.gettempdir())
+    clock_path = os.path.join(clock_dir, f"bench_clocks_rank{rank}.csv")
     os.makedirs(os.path.dirname(clock_path), exist_ok=True)
     barrier(world)
     torch.cuda.synchronize()
