@@ -107,3 +107,21 @@ def test_decode_reports_causal_slice_longer_than_max_seqlen_q():
     assert int(status.item()) & ffa.STATUS_BAD_RANGE
     # every slice was dropped: every row is empty (O = 0, LSE = -inf)
     assert torch.count_nonzero(o).item() == 0 and bool(torch.isinf(l).all())
+
+
+@pytest.mark.parametrize("hq,hkv,cap", [(12, 4, 30.0), (3, 1, 0.0), (16, 16, 5.0)])
+def test_decode_softcap_and_odd_groups(hq, hkv, cap):
+    # odd G (3 query heads per key/value head) packs all G heads as rows; G = 1 is plain MHA
+    qr, kr, ty, nq, nk = _batch(9, 2, 20 + hq, 150, 1800)
+    g = W.make_generator(120 + hq)
+    d = 128
+    q = torch.randn(nq, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    scale = 0.75 / math.sqrt(d)
+    o, l = ffa.ffa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, max_seqlen_q=2, softmax_scale=scale,
+                              softcap=cap)
+    torch.cuda.synchronize()
+    ro, rl = O.forward(q, k, v, qr, kr, ty, softmax_scale=scale, softcap=cap)
+    assert_out_close(to64(o), ro)
+    assert_lse_close(to64(l), rl)

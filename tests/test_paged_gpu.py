@@ -106,3 +106,19 @@ def test_paged_entry_outside_pool_is_reported():
     ro, rl = O.forward(q, k0, v0, [[0, nq]], [[0, nk]], [O.FULL])
     assert_out_close(to64(o_p), ro)
     assert_lse_close(to64(l_p), rl)
+
+
+def test_paged_with_alibi():
+    nq, nk, hq, hkv, d, page = 400, 1100, 8, 2, 128, 64
+    q, k, v = _draw(nq, nk, hq, hkv, d, 41)
+    qr, kr, ty = W.random_slices(nq, nk, 6, 41)
+    kp, vp, table = _pool(k, v, page, 2, 42)
+    slopes = torch.tensor([2.0 ** -(h + 5) for h in range(hq)], dtype=torch.float32)
+    o_p, l_p = ffa.ffa_fwd_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), nk, qr, kr, ty,
+                                 alibi_slopes=slopes.cuda())
+    o_u, l_u = ffa.ffa_fwd(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, alibi_slopes=slopes.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(o_p, o_u) and torch.equal(l_p, l_u)
+    ro, rl = O.forward(q, k, v, qr, kr, ty, alibi_slopes=slopes.numpy())
+    assert_out_close(to64(o_p), ro)
+    assert_lse_close(to64(l_p), rl)
