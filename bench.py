@@ -265,7 +265,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local: int):
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out, lse, dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p, do_p, qr_h, kr_h, ty_h))
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    E = max(3, min(K, 6))
+    E = max(3, K)  # pipeline fill (first upload) and drain (last download) amortised over K steps
     sets = []
     for _ in range(2):
         ins = [torch.empty_like(t) for t in (q, k, v, do, qr, kr, ty)]
