@@ -284,9 +284,31 @@ __device__ void counting_sort_desc(const int* __restrict__ len, int n, int max_l
     run += h;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int pos = atomicAdd(&hist[min(max(len[i], 0), max_len)], 1);
-    order[pos] = i;
+  // Placement is stable (equal lengths keep ascending index order), so items of similar
+  // length that run at the same time are neighbours: for the backward, CTAs on neighbouring
+  // key tiles add into neighbouring query tiles, which keeps the dq accumulator's working set
+  // in L2.  Items go in chunks of blockDim.x, the warps of a chunk one after another; inside a
+  // warp, lanes with the same length rank by lane order.
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int c = i < n ? min(max(len[i], 0), max_len) : -1;
+    for (int ww = 0; ww < nw; ++ww) {
+      if (w == ww) {
+        const unsigned peers = __match_any_sync(0xffffffffu, c);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int first = __ffs(peers) - 1;
+        int start = 0;
+        if (c >= 0) start = hist[c];
+        __syncwarp();
+        if (c >= 0) {
+          order[start + rank] = i;
+          if (lane == first) hist[c] = start + __popc(peers);
+        }
+        __syncwarp();
+      }
+      __syncthreads();
+    }
   }
 }
 
