@@ -16,12 +16,19 @@
 // heads of one GQA group over the same query tile (G even) or two adjacent query tiles of
 // one head (G odd).  Persistent grid (one CTA per SM), static longest-first snake schedule.
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads):
 //   warps 0-3  softmax warpgroup 0: row r of query tile 0 <-> TMEM lane r
 //   warps 4-7  softmax warpgroup 1: query tile 1
 //   warp 8     TMA producer (lane 0): Q tiles once per item, K/V tiles through a ring
 //   warp 9     MMA issuer (lane 0): S_t = Q_t K^T into TMEM, O_t += P_t V with P_t read
 //              from TMEM; owns the TMEM allocation
+//   warps 10-11 idle: they complete the producer warpgroup, so that each SM sub-partition
+//              (warp % 4) holds two softmax warps and one producer warp
+// Registers: launched at 168 per thread; the producer warpgroup gives registers back
+// (setmaxnreg.dec to kRegsProducer) and the softmax warpgroups take them
+// (setmaxnreg.inc to kRegsSoftmax).  A warp's registers come from its own sub-partition's
+// file, so the split must balance per sub-partition: 2 * kRegsSoftmax + kRegsProducer =
+// 3 * 168, which also equals the block's launch total per warp triple.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).  P_t is
 // written as bf16 over the first 64 columns of S_t.
 //
@@ -29,6 +36,9 @@
 // of a row moves only when a new tile's max exceeds it by more than kTau (p <= 2^kTau), and
 // only then is that row of O rescaled in TMEM.  Rows with no visible key so far use 0 as
 // the reference (safe softmax), so fully masked rows end with l = 0: O = 0, LSE = -inf.
+#include <cmath>
+#include <type_traits>
+
 #include "ffa_internal.h"
 #include "ffa_ptx.cuh"
 #include "../../include/ffa.h"
@@ -39,7 +49,10 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kRegsLaunch = 168, kRegsSoftmax = 200, kRegsProducer = 104;
+static_assert(2 * kRegsSoftmax + kRegsProducer == 3 * kRegsLaunch, "per sub-partition register split");
+static_assert(kThreads * kRegsLaunch <= 65536, "launch register file");
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 
@@ -66,6 +79,10 @@ struct FwdParams {
   float scale_log2;  // softmax_scale * log2(e)
   float cap_c;       // softcap * log2(e)
   float cap_k;       // 2 * softmax_scale * log2(e) / softcap
+  // capped logit in the log2 domain as an odd polynomial of the raw score s,
+  // x = s * (q0 + q1 s^2 + q2 s^4 + q3 s^6), valid for |s| <= cap_slim (< 0: never used)
+  float cap_q[4];
+  float cap_slim;
   PlanView plan;
   __nv_bfloat16* out;
   float* lse;
@@ -279,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
+    reg_alloc<kRegsSoftmax>();
     const int wg = warp >> 2, q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
@@ -335,13 +353,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool masked = (cls != FFA_TILE_FULL) || (kt * kTile + kTile > p.nk);
         // ALiBi in the log2 domain: slope * log2(e) * (key - row) = bbase + slope * log2(e) * c
         const float bbase = kBias ? slope_log2 * static_cast<float>(kt * kTile - row) : 0.0f;
+        // Softcap on a fully visible tile: when every raw score of the warp's rows lies where
+        // the tanh polynomial holds, the logits are formed inside the exponential pass (FMA
+        // pipe only), and the row max is the polynomial at the raw max, the transform being
+        // increasing there.  Otherwise (and on masked tiles) the exact transform runs first.
+        constexpr bool kPolyCap = kCap && !kBias;
+        bool poly = false;
+        float mx = -INFINITY;
+        if (kPolyCap && !masked) {
+          float hi[4], lo[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            hi[u] = -INFINITY;
+            lo[u] = INFINITY;
+          }
+#pragma unroll
+          for (int c = 0; c < 128; c += 2) {
+            const float a = __uint_as_float(sv[c >> 5][c & 31]), b = __uint_as_float(sv[c >> 5][(c & 31) + 1]);
+            hi[(c >> 1) & 3] = fmax3(hi[(c >> 1) & 3], a, b);
+            lo[(c >> 1) & 3] = fmin3(lo[(c >> 1) & 3], a, b);
+          }
+          const float smax = fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3]));
+          const float smin = fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3]));
+          poly = __all_sync(0xffffffffu, fmaxf(smax, -smin) <= p.cap_slim);
+          if (poly) {
+            const float t = smax * smax;
+            mx = smax * fmaf(fmaf(fmaf(p.cap_q[3], t, p.cap_q[2]), t, p.cap_q[1]), t, p.cap_q[0]);
+          }
+        }
         // row max: eight independent partial maxima when the logits are formed first (a
         // longer transform per element), one chain otherwise (measured faster there)
         constexpr int kMx = kPre ? 8 : 1;
         float mxs[kMx];
 #pragma unroll
         for (int u = 0; u < kMx; ++u) mxs[u] = -INFINITY;
-        if (masked) {
+        if (poly) {
+          // the maximum is known
+        } else if (masked) {
           uint32_t w[4];
           if (ivl_ok && cls != FFA_TILE_FULL) {
             const int c0 = kt * kTile;
@@ -379,9 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mxs[c % kMx] = fmaxf(mxs[c % kMx], x);
           }
         }
-        float mx = mxs[0];
+        if (!poly) {
+          mx = mxs[0];
 #pragma unroll
-        for (int u = 1; u < kMx; ++u) mx = fmaxf(mx, mxs[u]);
+          for (int u = 1; u < kMx; ++u) mx = fmaxf(mx, mxs[u]);
+        }
         const float m_tile = kPre ? mx : mx * p.scale_log2;
         const bool need = m_tile > m_run + kTau;
         const bool rescale = need && (m_run != -INFINITY);
@@ -398,20 +448,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 sumr2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
         const float sc = kPre ? 1.0f : p.scale_log2;
         const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(neg_m, neg_m);
+        auto exp_pass = [&](auto poly_tag) {
+          constexpr bool kP = decltype(poly_tag)::value;
+          float2 q[4];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t pk[16];
+          for (int i = 0; i < 4; ++i) q[i] = kP ? make_float2(p.cap_q[i], p.cap_q[i]) : make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 y = fma2(make_float2(__uint_as_float(sv[c4][2 * k]), __uint_as_float(sv[c4][2 * k + 1])), sc2,
-                                  nm2);
-            const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
-            sum2[k & 1] = add2(sum2[k & 1], make_float2(p0, p1));
-            pk[k] = pack_bf16x2(p0, p1);
-            sumr2[k & 1] = add2(sumr2[k & 1], make_float2(__uint_as_float(pk[k] << 16),
-                                                          __uint_as_float(pk[k] & 0xffff0000u)));
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float2 s2 = make_float2(__uint_as_float(sv[c4][2 * k]), __uint_as_float(sv[c4][2 * k + 1]));
+              float2 y;
+              if constexpr (kP) {
+                const float2 t = mul2(s2, s2);
+                const float2 w = fma2(fma2(fma2(q[3], t, q[2]), t, q[1]), t, q[0]);
+                y = fma2(s2, w, nm2);
+              } else {
+                y = fma2(s2, sc2, nm2);
+              }
+              const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+              sum2[k & 1] = add2(sum2[k & 1], make_float2(p0, p1));
+              pk[k] = pack_bf16x2(p0, p1);
+              sumr2[k & 1] = add2(sumr2[k & 1], make_float2(__uint_as_float(pk[k] << 16),
+                                                            __uint_as_float(pk[k] & 0xffff0000u)));
+            }
+            tmem_st16(tS + 16 * c4, pk);
           }
-          tmem_st16(tS + 16 * c4, pk);
+        };
+        if constexpr (kPolyCap) {
+          if (poly) {
+            exp_pass(std::true_type{});
+          } else {
+            exp_pass(std::false_type{});
+          }
+        } else {
+          exp_pass(std::false_type{});
         }
         l_run += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
         r_run += (sumr2[0].x + sumr2[0].y) + (sumr2[1].x + sumr2[1].y);
@@ -482,7 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok) record_abort(abort_flag, p.status);
-  } else if (warp == kWarpTma) {
+  } else {
+  reg_dealloc<kRegsProducer>();
+  if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it_cnt = 0;
@@ -574,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, false, false);
@@ -643,6 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   }
+  }  // producer warpgroup
 
   tc_fence_before();
   __syncthreads();
@@ -710,6 +785,34 @@ __global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
   if (lse_writer) p.lse[static_cast<size_t>(h) * p.nq + row] = mx + lg2_approx(wsum) * kLn2;
 }
 
+
+// tanh(y) / y ~ c0 + c1 y^2 + c2 y^4 + c3 y^6 on |y| <= kTanhPolyY.  The coefficients were
+// fitted in float64 for minimax relative error (least squares on Chebyshev nodes, reweighted
+// by the error until it equioscillates); evaluated by Horner's rule in float32 the product
+// y * P(y^2) stays within 1.6e-7 of tanh(y), relative, over the whole interval.
+constexpr double kTanhPolyY = 0.375;
+constexpr double kTanhPoly[4] = {9.999999421e-01, -3.333199304e-01, 1.328484108e-01, -4.828819503e-02};
+
+// The capped logit in the log2 domain, x(s) = C tanh(a s) with a = scale / softcap and
+// C = softcap * log2(e), folded into one odd polynomial of the raw score:
+// x(s) = s * sum_i q_i s^{2i}, q_i = C c_i a^{2i+1}, for |s| <= kTanhPolyY / a.  Left unused
+// (cap_slim < 0) when a folded coefficient would not be a normal float.
+void set_cap_poly(FwdParams& p, float scale, float softcap) {
+  p.cap_slim = -1.0f;
+  for (int i = 0; i < 4; ++i) p.cap_q[i] = 0.0f;
+  if (!(softcap > 0.0f) || !(scale > 0.0f)) return;
+  const double a = static_cast<double>(scale) / softcap;
+  const double C = static_cast<double>(softcap) * 1.4426950408889634;
+  float q[4];
+  for (int i = 0; i < 4; ++i) {
+    q[i] = static_cast<float>(C * kTanhPoly[i] * std::pow(a, 2 * i + 1));
+    if (!std::isnormal(q[i])) return;
+  }
+  const float slim = static_cast<float>(kTanhPolyY / a * (1.0 - 1e-6));
+  if (!std::isfinite(slim) || !std::isfinite(slim * slim)) return;
+  for (int i = 0; i < 4; ++i) p.cap_q[i] = q[i];
+  p.cap_slim = slim;
+}
 template <int D, bool kCap, bool kBias>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   using SM = FwdSmem<D>;
@@ -737,6 +840,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * kLog2e;
   p.cap_c = a.softcap * kLog2e;
   p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
+  set_cap_poly(p, a.scale, a.softcap);
   p.plan = a.plan;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
