@@ -139,6 +139,27 @@ def test_sliding_softcap_full_size_sampled():
 
 
 @pytest.mark.slow
+def test_documents_full_size_sampled():
+    """The document-masked batch at full size (its config is forward-only; the backward is
+    checked as well): sampled rows around document boundaries and random keys."""
+    w = W.get("docs_16k")
+    q, k, v, do = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed)
+    dq, dk, dv = _gpu_grads(q, k, v, do, w.q_ranges, w.k_ranges, w.types)
+    starts = np.cumsum([0] + list(w.doc_lengths))[:-1]
+    g = np.random.default_rng(6)
+    edges = np.concatenate([starts, starts + 1, starts[1:] - 1, [w.total - 1]])
+    rows = np.unique(np.concatenate([edges, g.integers(0, w.total, 16)]))
+    rq, _, _ = O.backward(q, k, v, do, w.q_ranges, w.k_ranges, w.types, rows=rows)
+    assert_grad_close(to64(dq[rows]), rq, "dq rows")
+    keys = np.unique(np.concatenate([starts, starts[1:] - 1, g.integers(0, w.total, 12)]))
+    _, rk, rv = O.backward(q, k, v, do, w.q_ranges, w.k_ranges, w.types, keys=keys)
+    assert_grad_close(to64(dk[keys]), rk, "dk keys")
+    assert_grad_close(to64(dv[keys]), rv, "dv keys")
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+
+
+@pytest.mark.slow
 def test_long_causal_full_size_sampled_and_sum_property():
     w = W.get("long_causal_64k_prefix")
     q, k, v, do = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed)
