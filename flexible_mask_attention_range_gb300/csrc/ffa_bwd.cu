@@ -69,6 +69,9 @@ struct BwdParams {
   float scale;
   float scale_log2;
   float cap_c, cap_k, inv_cap_c;
+  // capped logit as an odd polynomial of the raw score, valid for |s| <= cap_slim (< 0: unused)
+  float cap_q[4];
+  float cap_slim;
   PlanView plan;
   const float* lse2;
   const float* rowD;
@@ -348,13 +351,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           reg_fence(sv);
           uint32_t pk[16];
+          // Softcap without a bias: when every raw score of this chunk over the warp lies where
+          // the tanh polynomial holds, the capped logits come from the polynomial (FMA pipe,
+          // two columns per packed instruction); otherwise from the exact form.
+          auto k4_loop = [&](auto ptag) {
+          constexpr bool kPoly = decltype(ptag)::value;
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
             const float4 l4 = *reinterpret_cast<const float4*>(stat + c0 + 32 * c + 4 * k4);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
             // the row statistics are stored negated: -LSE * log2(e) (see ffa_bwd_pre)
             float pv[4], pd[4];
-            if (kCap) {
+            if (kCap && kPoly) {
+              const float2 invc2 = make_float2(p.inv_cap_c, p.inv_cap_c), one2 = make_float2(1.0f, 1.0f);
+              const float2 q0 = make_float2(p.cap_q[0], p.cap_q[0]), q1 = make_float2(p.cap_q[1], p.cap_q[1]);
+              const float2 q2 = make_float2(p.cap_q[2], p.cap_q[2]), q3 = make_float2(p.cap_q[3], p.cap_q[3]);
+#pragma unroll
+              for (int hp = 0; hp < 2; ++hp) {
+                const int col0 = c0 + 32 * c + 4 * k4 + 2 * hp;
+                const float2 s2 = make_float2(__uint_as_float(sv[4 * k4 + 2 * hp]), __uint_as_float(sv[4 * k4 + 2 * hp + 1]));
+                const float2 t = mul2(s2, s2);
+                const float2 x = mul2(s2, fma2(fma2(fma2(q3, t, q2), t, q1), t, q0));
+                const float2 y = add2(x, make_float2(lv[2 * hp], lv[2 * hp + 1]));
+                float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+                const float2 th = mul2(x, invc2);
+                const float2 dd = mul2(make_float2(p0, p1), fma2(make_float2(-th.x, -th.y), th, one2));
+                float d0 = dd.x, d1 = dd.y;
+                if (kM && mk) {
+                  if (!((w[col0 >> 5] >> (col0 & 31)) & 1u)) p0 = d0 = 0.0f;
+                  if (!((w[(col0 + 1) >> 5] >> ((col0 + 1) & 31)) & 1u)) p1 = d1 = 0.0f;
+                }
+                pv[2 * hp] = p0;
+                pv[2 * hp + 1] = p1;
+                pd[2 * hp] = d0;
+                pd[2 * hp + 1] = d1;
+              }
+            } else if (kCap) {
 #pragma unroll
               for (int h4 = 0; h4 < 4; ++h4) {
                 const int col = c0 + 32 * c + 4 * k4 + h4;
@@ -398,6 +430,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               pp[16 * c + 2 * k4] = pk[2 * k4];
               pp[16 * c + 2 * k4 + 1] = pk[2 * k4 + 1];
             }
+          }
+          };
+          if constexpr (kCap && !kBias) {
+            float hi[2] = {-INFINITY, -INFINITY}, lo[2] = {INFINITY, INFINITY};
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float a = __uint_as_float(sv[i]), b = __uint_as_float(sv[i + 1]);
+              hi[(i >> 1) & 1] = fmax3(hi[(i >> 1) & 1], a, b);
+              lo[(i >> 1) & 1] = fmin3(lo[(i >> 1) & 1], a, b);
+            }
+            if (__all_sync(0xffffffffu, fmaxf(fmaxf(hi[0], hi[1]), -fminf(lo[0], lo[1])) <= p.cap_slim)) {
+              k4_loop(std::true_type{});
+            } else {
+              k4_loop(std::false_type{});
+            }
+          } else {
+            k4_loop(std::false_type{});
           }
           tmem_st16(tS + 16 * c, pk);
         }
@@ -796,6 +845,7 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   p.cap_c = a.softcap * kLog2e;
   p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
   p.inv_cap_c = a.softcap > 0.0f ? 1.0f / p.cap_c : 0.0f;
+  fold_cap_poly(a.scale, a.softcap, p.cap_q, &p.cap_slim);
   p.plan = a.plan;
   p.lse2 = a.lse2;
   p.rowD = a.rowD;

@@ -786,33 +786,6 @@ __global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
 }
 
 
-// tanh(y) / y ~ c0 + c1 y^2 + c2 y^4 + c3 y^6 on |y| <= kTanhPolyY.  The coefficients were
-// fitted in float64 for minimax relative error (least squares on Chebyshev nodes, reweighted
-// by the error until it equioscillates); evaluated by Horner's rule in float32 the product
-// y * P(y^2) stays within 1.6e-7 of tanh(y), relative, over the whole interval.
-constexpr double kTanhPolyY = 0.375;
-constexpr double kTanhPoly[4] = {9.999999421e-01, -3.333199304e-01, 1.328484108e-01, -4.828819503e-02};
-
-// The capped logit in the log2 domain, x(s) = C tanh(a s) with a = scale / softcap and
-// C = softcap * log2(e), folded into one odd polynomial of the raw score:
-// x(s) = s * sum_i q_i s^{2i}, q_i = C c_i a^{2i+1}, for |s| <= kTanhPolyY / a.  Left unused
-// (cap_slim < 0) when a folded coefficient would not be a normal float.
-void set_cap_poly(FwdParams& p, float scale, float softcap) {
-  p.cap_slim = -1.0f;
-  for (int i = 0; i < 4; ++i) p.cap_q[i] = 0.0f;
-  if (!(softcap > 0.0f) || !(scale > 0.0f)) return;
-  const double a = static_cast<double>(scale) / softcap;
-  const double C = static_cast<double>(softcap) * 1.4426950408889634;
-  float q[4];
-  for (int i = 0; i < 4; ++i) {
-    q[i] = static_cast<float>(C * kTanhPoly[i] * std::pow(a, 2 * i + 1));
-    if (!std::isnormal(q[i])) return;
-  }
-  const float slim = static_cast<float>(kTanhPolyY / a * (1.0 - 1e-6));
-  if (!std::isfinite(slim) || !std::isfinite(slim * slim)) return;
-  for (int i = 0; i < 4; ++i) p.cap_q[i] = q[i];
-  p.cap_slim = slim;
-}
 template <int D, bool kCap, bool kBias>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   using SM = FwdSmem<D>;
@@ -840,7 +813,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * kLog2e;
   p.cap_c = a.softcap * kLog2e;
   p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
-  set_cap_poly(p, a.scale, a.softcap);
+  fold_cap_poly(a.scale, a.softcap, p.cap_q, &p.cap_slim);
   p.plan = a.plan;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;

@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 
@@ -47,6 +48,35 @@ struct WsLayout {
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Softcap as a polynomial: tanh(y) / y ~ c0 + c1 y^2 + c2 y^4 + c3 y^6 on |y| <= kTanhPolyY.
+// The coefficients were fitted in float64 for minimax relative error (least squares on
+// Chebyshev nodes, reweighted by the error until it equioscillates); evaluated by Horner's
+// rule in float32 the product y * P(y^2) stays within 1.6e-7 of tanh(y), relative, over the
+// whole interval.
+constexpr double kTanhPolyY = 0.375;
+constexpr double kTanhPoly[4] = {9.999999421e-01, -3.333199304e-01, 1.328484108e-01, -4.828819503e-02};
+
+// The capped logit in the log2 domain, x(s) = C tanh(a s) with a = scale / softcap and
+// C = softcap * log2(e), folded into one odd polynomial of the raw score:
+// x(s) = s * sum_i q_i s^{2i}, q_i = C c_i a^{2i+1}, valid for |s| <= *slim.  *slim < 0 (the
+// polynomial unused) without softcap or when a folded coefficient would not be a normal float.
+inline void fold_cap_poly(float scale, float softcap, float (&q_out)[4], float* slim) {
+  *slim = -1.0f;
+  for (int i = 0; i < 4; ++i) q_out[i] = 0.0f;
+  if (!(softcap > 0.0f) || !(scale > 0.0f)) return;
+  const double a = static_cast<double>(scale) / softcap;
+  const double C = static_cast<double>(softcap) * 1.4426950408889634;
+  float q[4];
+  for (int i = 0; i < 4; ++i) {
+    q[i] = static_cast<float>(C * kTanhPoly[i] * std::pow(a, 2 * i + 1));
+    if (!std::isnormal(q[i])) return;
+  }
+  const float s = static_cast<float>(kTanhPolyY / a * (1.0 - 1e-6));
+  if (!std::isfinite(s) || !std::isfinite(s * s)) return;
+  for (int i = 0; i < 4; ++i) q_out[i] = q[i];
+  *slim = s;
+}
 
 inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int R) {
   WsLayout L;

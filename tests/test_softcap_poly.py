@@ -1,7 +1,7 @@
-"""The forward kernel's softcap polynomial (tanh(y)/y as a cubic in y^2 on |y| <= Y0, used
-on fully visible tiles whose scores all lie in range) against float64 tanh.  The constants
-are read from the kernel source; the evaluation repeats the kernel's float32 Horner order,
-both in y and in the folded form in the raw score.  CPU only."""
+"""The kernels' softcap polynomial (tanh(y)/y as a cubic in y^2 on |y| <= Y0, used where all
+of a warp's scores lie in range) against float64 tanh.  The constants are read from the
+kernels' shared header; the evaluation repeats the kernels' float32 Horner order, both in y
+and in the folded form in the raw score.  CPU only."""
 import math
 import os
 import re
@@ -9,7 +9,7 @@ import re
 import numpy as np
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SRC = os.path.join(ROOT, "flexible_mask_attention_range_gb300", "csrc", "ffa_fwd.cu")
+SRC = os.path.join(ROOT, "flexible_mask_attention_range_gb300", "csrc", "ffa_internal.h")
 LOG2E = 1.4426950408889634
 
 
