@@ -7,6 +7,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -42,6 +43,32 @@ def needs_build() -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
+def check_forward_registers(ptxas_log: str) -> None:
+    """The forward kernel rebalances registers between warpgroups (setmaxnreg); the split in
+    its source is exact for one launch register count (kRegsLaunch).  Refuse a build whose
+    forward kernels were given any other count: such a launch could wait forever."""
+    src = open(os.path.join(CSRC, "ffa_fwd.cu")).read()
+    want = int(re.search(r"kRegsLaunch = (\d+)", src).group(1))
+    found = []
+    current = None
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current is not None:
+            if "ffa_fwd_kernel" in current:
+                found.append(int(m.group(1)))
+            current = None
+    if not found:
+        raise RuntimeError("no register report for the forward kernels in the ptxas output")
+    bad = [n for n in found if n != want]
+    if bad:
+        raise RuntimeError(f"forward kernels built with {sorted(set(bad))} registers per thread; the register "
+                           f"split needs exactly {want}")
+
+
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
@@ -52,11 +79,15 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + flags
+        extra = ["-Xptxas", "-v"] if src == "ffa_fwd.cu" and not ptxas_info else []
+        cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + flags + extra
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
-        return obj, r.stdout + r.stderr
+        log = r.stdout + r.stderr
+        if src == "ffa_fwd.cu":
+            check_forward_registers(log)
+        return obj, log if (verbose or ptxas_info or not extra) else ""
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))

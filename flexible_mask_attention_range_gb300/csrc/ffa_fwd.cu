@@ -792,7 +792,14 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   static bool attr_set = false;
   auto kern = ffa_fwd_kernel<D, kCap, kBias>;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+    // The register split (setmaxnreg) is balanced for exactly kRegsLaunch registers per
+    // thread at launch; with any other count a softmax warp's increase could never be
+    // granted, so such a build is refused here rather than launched.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

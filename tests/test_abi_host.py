@@ -113,3 +113,16 @@ def test_decode_argument_checks(lib_path):
     slopes = ffa.FfaOptions(16)
     assert call(opts=ctypes.byref(slopes)) == 2                             # ALiBi not here
     assert call() == 4                                                      # then: no workspace
+
+
+def test_build_refuses_forward_kernels_with_another_register_count():
+    import flexible_mask_attention_range_gb300.build as b
+    ok_log = ("ptxas info    : Compiling entry function '_ZN3ffa14ffa_fwd_kernelILi128ELb0ELb0EEEvv' for 'sm_103a'\n"
+              "ptxas info    : Used 168 registers, used 1 barriers\n"
+              "ptxas info    : Compiling entry function '_ZN3ffa14ffa_fwd_mergeILi128EEEvv' for 'sm_103a'\n"
+              "ptxas info    : Used 40 registers\n")
+    b.check_forward_registers(ok_log)
+    with pytest.raises(RuntimeError):
+        b.check_forward_registers(ok_log.replace("Used 168", "Used 160"))
+    with pytest.raises(RuntimeError):
+        b.check_forward_registers("no report at all\n")
