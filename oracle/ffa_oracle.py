@@ -18,12 +18,13 @@ each row's whole key set):
     Optimized Attention Kernels", section 3 (Composability): masks combine by logical OR,
     e.g. prefix OR causal gives PrefixLM.  A (query, key) pair is visible once, no matter
     how many slices cover it (union semantics).
-  * Softcapping limits logit growth (same paper, section 2, attention variants); the
-    reading taken here: x = softcap * tanh(scale * q.k / softcap), softcap = 0 disables it.
+  * Softcapping (same paper, section 2, attention variants) keeps every logit inside
+    (-softcap, softcap); the reading taken here: x = softcap * tanh(scale * q.k / softcap),
+    softcap = 0 disables it.
   * Safe softmax (same paper, section 1): rows with no visible key produce O = 0 and
     LSE = -inf instead of NaN.
-  * ALiBi score modification (same paper, sections 2 and 3.1: ALiBi adds a distance-based,
-    position-dependent bias to the score): optional per-query-head slopes; reading taken
+  * ALiBi score modification (same paper, sections 2 and 3.1: each score gets a bias that
+    grows with the distance between query and key): optional per-query-head slopes; reading taken
     here: x_ij = softcap(scale * q.k) + slope_h * (j - i) with i, j the packed token
     positions (the distance between two tokens of one document equals their in-document
     distance).
