@@ -126,3 +126,32 @@ def test_build_refuses_forward_kernels_with_another_register_count():
         b.check_forward_registers(ok_log.replace("Used 168", "Used 160"))
     with pytest.raises(RuntimeError):
         b.check_forward_registers("no report at all\n")
+
+
+def test_options_argument_checks(lib_path):
+    """ffa_fwd_ex / ffa_bwd_ex: reserved option fields must be zero and the ALiBi slope array
+    4-byte aligned; valid options (or none) pass on to the workspace check."""
+    L = ffa.lib()
+    p = ctypes.c_void_p(16)
+    s = ffa.FfaShape(256, 256, 2, 1, 64)
+
+    def fwd(opts):
+        return L.ffa_fwd_ex(ctypes.byref(s), p, p, p, p, p, p, 1, -1.0, 0.0, p, p, None, 0, None, None, opts)
+
+    def bwd(opts):
+        return L.ffa_bwd_ex(ctypes.byref(s), p, p, p, p, p, p, p, p, p, 1, -1.0, 0.0, p, p, p, None, 0, None, None,
+                            opts)
+
+    for call in (fwd, bwd):
+        assert call(None) == 4
+        assert call(ctypes.byref(ffa.FfaOptions())) == 4
+        det = ffa.FfaOptions()
+        det.deterministic = 1
+        assert call(ctypes.byref(det)) == 4
+        for i in range(7):
+            bad = ffa.FfaOptions()
+            bad.reserved[i] = 1
+            assert call(ctypes.byref(bad)) == 1
+        mis = ffa.FfaOptions()
+        mis.alibi_slopes = 18
+        assert call(ctypes.byref(mis)) == 1
