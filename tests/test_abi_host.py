@@ -155,3 +155,26 @@ def test_options_argument_checks(lib_path):
         mis = ffa.FfaOptions()
         mis.alibi_slopes = 18
         assert call(ctypes.byref(mis)) == 1
+
+
+def test_noalloc_host_checks(lib_path):
+    """ffa_fwd_noalloc refuses, before any launch, shapes whose forward workspace exceeds its
+    fixed scratch (FFA_ERR_TOO_LARGE) and the usual invalid arguments."""
+    L = ffa.lib()
+    p = ctypes.c_void_p(16)
+
+    def call(shape, ptr=p, softcap=0.0, R=1):
+        return L.ffa_fwd_noalloc(ctypes.byref(shape), ptr, ptr, ptr, ptr, ptr, ptr, R, -1.0, softcap, ptr, ptr,
+                                 None, None)
+
+    n = 300000
+    assert ffa.ffa_fwd_workspace_size(n, n, 2, 1, 64, 1) > ffa.FWD_NOALLOC_SCRATCH_BYTES
+    rc = call(ffa.FfaShape(n, n, 2, 1, 64))
+    assert rc == ffa.ERR_TOO_LARGE
+    assert "scratch" in ffa.ffa_status_string(rc)
+    s = ffa.FfaShape(256, 256, 2, 1, 64)
+    assert call(ffa.FfaShape(256, 256, 3, 2, 64)) == 1       # Hq % Hkv
+    assert call(ffa.FfaShape(256, 256, 2, 1, 96)) == 2       # head_dim
+    assert call(s, softcap=-1.0) == 1
+    assert call(s, ptr=ctypes.c_void_p(18)) == 1              # misaligned
+    assert call(s, R=-1) == 1
