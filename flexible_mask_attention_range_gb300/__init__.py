@@ -119,6 +119,16 @@ def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def _cuda_device(t, name: str = "q") -> torch.device:
+    """The device of the call: a CUDA device, else an error (the kernels take device pointers;
+    there is no CPU path)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device}); there is no CPU path")
+    return t.device
+
+
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device, shape=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -175,7 +185,7 @@ def ffa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_range
             alibi_slopes: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """out [Nq,Hq,d] bf16 and lse [Hq,Nq] float32 (natural log); see include/ffa.h.
     ``alibi_slopes`` (float32 [Hq]) adds slope_h * (key - query position) to the scores."""
-    dev = q.device
+    dev = _cuda_device(q)
     nq, hq, d = q.shape
     nk, hkv = k.shape[0], k.shape[1]
     _need(q, "q", torch.bfloat16, dev)
@@ -219,7 +229,7 @@ def ffa_fwd_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
     [n_pages, page_size, Hkv, d] pools and ``page_table`` (int32 [ceil(total_k / page_size)])
     maps each logical page of the ``total_k`` keys to a physical page; ranges, masks and
     results use logical positions (see include/ffa.h)."""
-    dev = q.device
+    dev = _cuda_device(q)
     nq, hq, d = q.shape
     n_pages, page_size, hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
     _need(q, "q", torch.bfloat16, dev)
@@ -264,7 +274,7 @@ def ffa_fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, 
     processed as rows of one problem.  Dense cache: k, v [Nk, Hkv, d].  Paged cache: k, v are
     [n_pages, page_size, Hkv, d] pools, ``page_table`` int32 and ``total_k`` the logical key
     count.  ``max_seqlen_q`` bounds the query tokens of any CAUSAL slice."""
-    dev = q.device
+    dev = _cuda_device(q)
     nq, hq, d = q.shape
     _need(q, "q", torch.bfloat16, dev)
     if page_table is None:
@@ -311,7 +321,7 @@ def ffa_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges,
     time: the library's fixed device scratch array is used instead (see include/ffa.h).
     Pass preallocated ``out``/``lse`` (and device-resident ranges) to keep the call itself
     free of allocations."""
-    dev = q.device
+    dev = _cuda_device(q)
     nq, hq, d = q.shape
     nk, hkv = k.shape[0], k.shape[1]
     _need(q, "q", torch.bfloat16, dev)
@@ -341,7 +351,7 @@ def ffa_bwd(q, k, v, out, lse, dout, q_ranges, k_ranges, attn_type_map,
             deterministic: bool = False):
     """Gradients (dq, dk, dv) of sum(out * dout); see include/ffa.h.  ``deterministic``
     orders the dq additions so the results are bit-reproducible."""
-    dev = q.device
+    dev = _cuda_device(q)
     nq, hq, d = q.shape
     nk, hkv = k.shape[0], k.shape[1]
     _need(q, "q", torch.bfloat16, dev)
@@ -386,6 +396,8 @@ def ffa_plan_tiles(total_q: int, total_k: int, q_ranges, k_ranges, attn_type_map
                    head_dim: int = 64, status: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Tile classes uint8 [ceil(Nq/128), ceil(Nk/128)] computed by the device planner."""
     dev = torch.device(device)
+    if dev.type != "cuda":
+        raise ValueError(f"device must be a CUDA device (got {dev}); there is no CPU path")
     qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
     R = qr.shape[0]
     shp = _shape(total_q, total_k, num_heads_q, num_heads_kv, head_dim)
@@ -421,6 +433,6 @@ def flex_flash_attn_func(q, k, v, q_ranges, k_ranges, attn_type_map, max_seqlen_
 
     The gradient flows through `out` only (the lse output is treated as non-differentiable).
     """
-    dev = q.device
+    dev = _cuda_device(q)
     qr, kr, ty = _ranges(q_ranges, k_ranges, attn_type_map, dev)
     return _FlexFlashAttn.apply(q, k, v, qr, kr, ty, softmax_scale, softcap)

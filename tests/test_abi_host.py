@@ -178,3 +178,26 @@ def test_noalloc_host_checks(lib_path):
     assert call(s, softcap=-1.0) == 1
     assert call(s, ptr=ctypes.c_void_p(18)) == 1              # misaligned
     assert call(s, R=-1) == 1
+
+
+def test_binding_refuses_cpu_tensors(lib_path):
+    """The kernels take device pointers: every entry point rejects host tensors up front."""
+    import torch
+    q = torch.randn(256, 2, 64).to(torch.bfloat16)
+    k = torch.randn(256, 1, 64).to(torch.bfloat16)
+    lse = torch.zeros(2, 256)
+    sl = ([(0, 256)], [(0, 256)], [1])
+    pool = torch.zeros(2, 128, 1, 64, dtype=torch.bfloat16)
+    table = torch.zeros(2, dtype=torch.int32)
+    calls = [
+        lambda: ffa.ffa_fwd(q, k, k, *sl),
+        lambda: ffa.ffa_bwd(q, k, k, q, lse, q, *sl),
+        lambda: ffa.ffa_fwd_noalloc(q, k, k, *sl),
+        lambda: ffa.ffa_fwd_paged(q, pool, pool, table, 256, *sl),
+        lambda: ffa.ffa_fwd_decode(q, k, k, *sl, max_seqlen_q=256),
+        lambda: ffa.flex_flash_attn_func(q, k, k, *sl),
+        lambda: ffa.ffa_plan_tiles(256, 256, *sl, device="cpu"),
+    ]
+    for c in calls:
+        with pytest.raises(ValueError, match="CUDA"):
+            c()
