@@ -322,10 +322,15 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local: int):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, world)
     e2e_value = world * (fl_fwd + fl_bwd) / (e2e_ms * 1e-3) / 1e12
 
-    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1900.0)))
     bwd_tf = fl_bwd / (bwd_ms * 1e-3) / 1e12
     fwd_tf = fl_fwd / (fwd_ms * 1e-3) / 1e12
-    traffic = read_profile_traffic(w.name)
+    # headline peak: the burst cuBLAS figure when the SM clock held its maximum during the
+    # timed region (the condition the burst figure was measured under), else the sustained one
+    peak_burst = float(peaks.get("bf16_tflops", 1900.0))
+    peak_sust = float(peaks.get("bf16_tflops_sustained", peak_burst))
+    at_max = (clocks.get("sm_mhz") is not None and clocks.get("sm_max_mhz")
+              and clocks["sm_mhz"] >= 0.97 * clocks["sm_max_mhz"])
+    peak_t, peak_kind = (peak_burst, "bf16_tflops (burst)") if at_max else (peak_sust, "bf16_tflops_sustained")
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
@@ -338,13 +343,17 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local: int):
         "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
         "fwd_kernel_ms": round(fwd_ms, 4), "bwd_kernel_ms": round(bwd_ms, 4),
         "frac_of_peak": {"fwd": round(fwd_tf / peak_t, 4), "bwd": round(bwd_tf / peak_t, 4),
-                         "step": round(value / world / peak_t, 4), "peak": f"bf16_tflops_sustained of {peak_src}"},
+                         "step": round(value / world / peak_t, 4), "peak": f"{peak_kind} of {peak_src}",
+                         "fwd_of_burst": round(fwd_tf / peak_burst, 4), "bwd_of_burst": round(bwd_tf / peak_burst, 4),
+                         "fwd_of_sustained": round(fwd_tf / peak_sust, 4),
+                         "bwd_of_sustained": round(bwd_tf / peak_sust, 4)},
         "roofline": {"kernel": "ffa_bwd_kernel", "bound": "tensor", "achieved": round(bwd_tf, 2),
                      "peak": peak_t, "unit": "TFLOP/s", "frac": round(bwd_tf / peak_t, 4),
-                     "traffic": traffic.get("ffa_bwd_kernel"), "peak_source": f"{peak_src} sustained bf16"},
+                     "traffic": kernel_traffic(w.name, "ffa_bwd_kernel"),
+                     "peak_source": f"{peak_kind} of {peak_src} (median SM clock {clocks.get('sm_mhz')} MHz)"},
         "roofline_fwd": {"kernel": "ffa_fwd_kernel", "bound": "tensor", "achieved": round(fwd_tf, 2),
                          "peak": peak_t, "unit": "TFLOP/s", "frac": round(fwd_tf / peak_t, 4),
-                         "traffic": traffic.get("ffa_fwd_kernel")},
+                         "traffic": kernel_traffic(w.name, "ffa_fwd_kernel")},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4), "copies": "pinned, own streams, overlapped with compute"},
         "gpu_launches": K * GPU_LAUNCHES_PER_STEP,
@@ -357,21 +366,123 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local: int):
 GPU_LAUNCHES_PER_STEP = 4 + 6
 
 
-def read_profile_traffic(workload: str):
-    """Per-launch DRAM bytes of the main kernels from the committed ncu summary table
-    (profiles/traffic.md rows `| workload | kernel | bytes |`), if any."""
-    p = os.path.join(ROOT, "profiles", "traffic.md")
-    out = {}
-    if not os.path.exists(p):
-        return out
-    for line in open(p):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) == 3 and cells[0] == workload:
-            try:
-                out[cells[1]] = float(cells[2])
-            except ValueError:
-                pass
-    return out
+def algorithmic_bytes(w: W.Workload):
+    """Bytes a pass must move at least: forward reads Q, K, V and writes O (bf16) and LSE
+    (f32); backward reads Q, K, V, O, dO, LSE and D and writes dQ, dK, dV."""
+    qb = w.total * w.hq * w.d * 2
+    kb = w.total * w.hkv * w.d * 2
+    row = w.total * w.hq * 4
+    fwd = qb + 2 * kb + qb + row
+    bwd = 3 * qb + 2 * kb + 2 * row + qb + 2 * kb
+    return fwd, bwd
+
+
+def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
+    """Every workload of the project timed alone on this GPU: the whole forward call (planner,
+    kernel, merge) and backward call (planner, preprocess, kernel, dq conversion) with CUDA
+    events on the launching stream, L2 flushed (a 256 MiB write) before every timed call;
+    medians of `iters` calls after `warm` untimed ones.  The main kernels alone are timed with
+    the library's event hook in the same calls."""
+    peak_b = float(peaks.get("bf16_tflops", 1900.0))
+    peak_s = float(peaks.get("bf16_tflops_sustained", peak_b))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    for name in W.ORDER:
+        w = W.get(name)
+        V = visible_pairs(w)
+        q_h, k_h, v_h, do_h, qr_h, kr_h, ty_h = make_inputs(w)
+        q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+        qr, kr, ty = (t.to(dev) for t in (qr_h, kr_h, ty_h))
+        out = torch.empty_like(q)
+        lse = torch.empty(w.hq, w.total, dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        R = qr.shape[0]
+        wsf = torch.empty(ffa.ffa_fwd_workspace_size(w.total, w.total, w.hq, w.hkv, w.d, R), dtype=torch.uint8,
+                          device=dev)
+        wsb = torch.empty(ffa.ffa_bwd_workspace_size(w.total, w.total, w.hq, w.hkv, w.d, R), dtype=torch.uint8,
+                          device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        t = {"fwd": [], "bwd": [], "fwd_kernel": [], "bwd_kernel": []}
+        for i in range(warm + iters):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+            for e in ev:
+                e.record()
+            flush.zero_()
+            ffa.ffa_set_kernel_events(ev[2], ev[3], None, None)
+            ev[0].record()
+            ffa.ffa_fwd(q, k, v, qr, kr, ty, w.softmax_scale, w.softcap, out=out, lse=lse, workspace=wsf, status=st)
+            ev[1].record()
+            if w.backward:
+                flush.zero_()
+                ffa.ffa_set_kernel_events(None, None, ev[6], ev[7])
+                ev[4].record()
+                ffa.ffa_bwd(q, k, v, out, lse, do, qr, kr, ty, w.softmax_scale, w.softcap, dq=dq, dk=dk, dv=dv,
+                            workspace=wsb, status=st)
+                ev[5].record()
+            ffa.ffa_set_kernel_events()
+            torch.cuda.synchronize()
+            if i >= warm:
+                t["fwd"].append(ev[0].elapsed_time(ev[1]))
+                t["fwd_kernel"].append(ev[2].elapsed_time(ev[3]))
+                if w.backward:
+                    t["bwd"].append(ev[4].elapsed_time(ev[5]))
+                    t["bwd_kernel"].append(ev[6].elapsed_time(ev[7]))
+        if int(st.item()) != 0:
+            raise RuntimeError(f"{name}: device status {int(st.item())}")
+        fb, bb = algorithmic_bytes(w)
+        e = {"visible_pairs": V, "tokens": w.total, "heads": f"{w.hq}/{w.hkv}", "d": w.d, "softcap": w.softcap,
+             "slices": len(w.types)}
+        for ph, flop, byt in (("fwd", 4.0 * w.d * w.hq * V, fb), ("bwd", 10.0 * w.d * w.hq * V, bb)):
+            if not t[ph]:
+                continue
+            ms = statistics.median(t[ph])
+            kms = statistics.median(t[ph + "_kernel"])
+            tf = flop / (ms * 1e-3) / 1e12
+            ktf = flop / (kms * 1e-3) / 1e12
+            e[ph] = {"ms": round(ms, 4), "us": round(ms * 1e3, 1), "tflops": round(tf, 2),
+                     "frac_burst": round(tf / peak_b, 4), "frac_sustained": round(tf / peak_s, 4),
+                     "hbm_gbs": round(byt / (ms * 1e-3) / 1e9, 1), "algorithmic_bytes": byt,
+                     "kernel_ms": round(kms, 4), "kernel_tflops": round(ktf, 2),
+                     "kernel_frac_burst": round(ktf / peak_b, 4)}
+        res[name] = e
+        del q, k, v, do, out, lse, dq, dk, dv, wsf, wsb
+        torch.cuda.empty_cache()
+    res["_timing"] = (f"median of {iters} calls after {warm} warm-up calls; L2 flushed (256 MiB write) before "
+                      "every timed call; 'ms' = whole call (planner included), 'kernel_ms' = main kernel alone; "
+                      f"peaks: burst {peak_b}, sustained {peak_s} TFLOP/s")
+    return res
+
+
+# DRAM bytes per launch of the main kernels (dram__bytes_read.sum + dram__bytes_write.sum from
+# one ncu capture of this benchmark's full-size workload; the capture command is in
+# profiles/).  Each entry carries the hash of the kernel's sources at capture time: once a
+# source changes the figure no longer describes the kernel, and `traffic` is reported null.
+TRAFFIC = {
+    # (workload, kernel): (bytes per launch, source hash at capture)
+    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1827558912 + 234647296, "629d7a67262ba57b"),
+    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (12691239168 + 6128407296, "f3a33f7eda8f2c7b"),
+    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541525760 + 237864192, "629d7a67262ba57b"),
+    ("sliding_32k_softcap", "ffa_bwd_kernel"): (6673673984 + 3498322176, "f3a33f7eda8f2c7b"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources that define a main kernel (its .cu plus the shared headers)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "flexible_mask_attention_range_gb300", "csrc")
+    unit = {"ffa_fwd_kernel": "ffa_fwd.cu", "ffa_bwd_kernel": "ffa_bwd.cu"}[kernel]
+    h = hashlib.sha256()
+    for f in (unit, "ffa_ptx.cuh", "ffa_internal.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(workload: str, kernel: str):
+    e = TRAFFIC.get((workload, kernel))
+    if e is None or e[1] != kernel_source_hash(kernel):
+        return None
+    return e[0]
 
 
 def oracle_sample(w: W.Workload, inputs, rows: np.ndarray):
@@ -423,6 +534,45 @@ def sample_rows(w: W.Workload, n: int, seed: int):
     return np.sort(g.choice(w.total, size=n, replace=False))
 
 
+def oracle_report(names, single_thread_names):
+    """The float64 oracle timed on this host's cores for each workload: the whole forward (and
+    backward where the workload has one) for the small ones, a seeded sample of 128 query rows
+    (forward + dq over each row's full key set) for the large ones, with the time of the full
+    pass extrapolated by useful flops.  Workloads in `single_thread_names` are timed again in a
+    child process restricted to one BLAS thread."""
+    import oracle as O
+    res = {"host_cores": os.cpu_count(), "blas_threads": cpu_threads()}
+    for name in names:
+        w = W.get(name)
+        V = visible_pairs(w)
+        q, k, v, do = W.draw_qkv(w.total, w.total, w.hq, w.hkv, w.d, w.seed)
+        full = (4.0 + (10.0 if w.backward else 0.0)) * w.d * w.hq * V
+        if w.total <= 16384:
+            t0 = time.perf_counter()
+            O.forward(q, k, v, w.q_ranges, w.k_ranges, w.types, softmax_scale=w.softmax_scale, softcap=w.softcap)
+            tf = time.perf_counter() - t0
+            tb = 0.0
+            if w.backward:
+                t0 = time.perf_counter()
+                O.backward(q, k, v, do, w.q_ranges, w.k_ranges, w.types, softmax_scale=w.softmax_scale,
+                           softcap=w.softcap)
+                tb = time.perf_counter() - t0
+            res[name] = {"kind": "full pass", "fwd_s": round(tf, 3), "bwd_s": round(tb, 3) if w.backward else None,
+                         "tflops": full / (tf + tb) / 1e12}
+        else:
+            rows = sample_rows(w, 128, 7)
+            dt, fl = oracle_sample(w, (q, k, v, do), rows)
+            res[name] = {"kind": "128 sampled rows, forward + dq", "sample_s": round(dt, 3), "tflops": fl / dt / 1e12,
+                         "extrapolated_full_fwd_bwd_s": round(dt * full / fl, 1)}
+    if single_thread_names:
+        env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-report", "--oracle-configs",
+                            ",".join(single_thread_names), "--oracle-single", ""], env=env, capture_output=True,
+                           text=True, check=True)
+        res["single_thread"] = json.loads(r.stdout.strip().splitlines()[-1])
+    return res
+
+
 def run_reference(args, w: W.Workload):
     inputs = make_inputs(w)[:4]
     rows_per_step = 24
@@ -456,7 +606,18 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_causal_64k_prefix", choices=sorted(W.ALL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--oracle-report", action="store_true",
+                    help="time the float64 oracle on the host cores for every workload and exit")
+    ap.add_argument("--oracle-configs", default=",".join(W.ORDER))
+    ap.add_argument("--oracle-single", default="tiny_256,page1_2048_gqa,docs_16k",
+                    help="workloads also timed on one BLAS thread (empty: none)")
     args = ap.parse_args()
+    if args.oracle_report:
+        names = [x for x in args.oracle_configs.split(",") if x]
+        single = [x for x in args.oracle_single.split(",") if x]
+        print(json.dumps(oracle_report(names, single)), flush=True)
+        return
     if args.warmup < 3:
         args.warmup = 3
     w = W.get(args.workload)
@@ -467,6 +628,9 @@ def main():
         return
     rank, world, local = dist_setup(args.gpus)
     result, inputs = run_ours(args, w, rank, world, local)
+    if world == 1 and not args.no_per_config:
+        import flexible_mask_attention_range_gb300 as ffa
+        result["per_config"] = per_config(ffa, torch.device("cuda", 0), load_peaks()[0])
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             n_rows = CPU_BASELINE_ROWS

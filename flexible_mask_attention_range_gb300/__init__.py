@@ -101,6 +101,13 @@ def lib():
     return _LIB
 
 
+def _on(dev: torch.device, fn, *args):
+    """Call a library entry point with ``dev`` current: the library resolves the device (SM
+    count, function attributes, the no-alloc scratch address) through the current device."""
+    with torch.cuda.device(dev):
+        return fn(*args)
+
+
 def _check(rc: int, what: str):
     if rc != 0:
         msg = lib().ffa_status_string(rc).decode()
@@ -207,13 +214,13 @@ def ffa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, k_range
         _need(status, "status", torch.int32, dev)
     scale = -1.0 if softmax_scale is None else float(softmax_scale)
     if alibi_slopes is None:
-        rc = lib().ffa_fwd(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty), R,
+        rc = _on(dev, lib().ffa_fwd, ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty), R,
                            scale, float(softcap), _ptr(out), _ptr(lse), _ptr(workspace),
                            workspace.numel(), _ptr(status), _stream(dev))
     else:
         _need(alibi_slopes, "alibi_slopes", torch.float32, dev, (hq,))
         opts = FfaOptions(alibi_slopes.data_ptr())
-        rc = lib().ffa_fwd_ex(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty), R,
+        rc = _on(dev, lib().ffa_fwd_ex, ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty), R,
                               scale, float(softcap), _ptr(out), _ptr(lse), _ptr(workspace),
                               workspace.numel(), _ptr(status), _stream(dev), ctypes.byref(opts))
     _check(rc, "ffa_fwd")
@@ -256,7 +263,7 @@ def ffa_fwd_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
     if alibi_slopes is not None:
         _need(alibi_slopes, "alibi_slopes", torch.float32, dev, (hq,))
         opts = FfaOptions(alibi_slopes.data_ptr())
-    rc = lib().ffa_fwd_paged(ctypes.byref(shp), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+    rc = _on(dev, lib().ffa_fwd_paged, ctypes.byref(shp), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
                              int(page_size), int(n_pages), _ptr(qr), _ptr(kr), _ptr(ty), R, scale, float(softcap),
                              _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev),
                              ctypes.byref(opts) if opts is not None else None)
@@ -269,11 +276,13 @@ def ffa_fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, 
                    page_table: Optional[torch.Tensor] = None, total_k: Optional[int] = None,
                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                    workspace: Optional[torch.Tensor] = None,
-                   status: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                   status: Optional[torch.Tensor] = None,
+                   alibi_slopes: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Decoding form of ffa_fwd (see include/ffa.h): the query heads of a key/value head are
     processed as rows of one problem.  Dense cache: k, v [Nk, Hkv, d].  Paged cache: k, v are
     [n_pages, page_size, Hkv, d] pools, ``page_table`` int32 and ``total_k`` the logical key
-    count.  ``max_seqlen_q`` bounds the query tokens of any CAUSAL slice."""
+    count.  ``max_seqlen_q`` bounds the query tokens of any CAUSAL slice.  ``alibi_slopes``
+    (float32 [Hq]) adds slope_h * (key - query position) as in ffa_fwd."""
     dev = _cuda_device(q)
     nq, hq, d = q.shape
     _need(q, "q", torch.bfloat16, dev)
@@ -305,10 +314,14 @@ def ffa_fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges, 
     if status is not None:
         _need(status, "status", torch.int32, dev)
     scale = -1.0 if softmax_scale is None else float(softmax_scale)
-    rc = lib().ffa_fwd_decode(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(page_table), int(page_size),
-                              int(n_pages), _ptr(qr), _ptr(kr), _ptr(ty), R, int(max_seqlen_q), scale,
-                              float(softcap), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-                              _ptr(status), _stream(dev), None)
+    opts = None
+    if alibi_slopes is not None:
+        _need(alibi_slopes, "alibi_slopes", torch.float32, dev, (hq,))
+        opts = FfaOptions(alibi_slopes.data_ptr())
+    rc = _on(dev, lib().ffa_fwd_decode, ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(page_table),
+             int(page_size), int(n_pages), _ptr(qr), _ptr(kr), _ptr(ty), R, int(max_seqlen_q), scale,
+             float(softcap), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev),
+             ctypes.byref(opts) if opts is not None else None)
     _check(rc, "ffa_fwd_decode")
     return out, lse
 
@@ -338,7 +351,7 @@ def ffa_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_ranges,
         _need(status, "status", torch.int32, dev)
     shp = _shape(nq, nk, hq, hkv, d)
     scale = -1.0 if softmax_scale is None else float(softmax_scale)
-    rc = lib().ffa_fwd_noalloc(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty),
+    rc = _on(dev, lib().ffa_fwd_noalloc, ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(ty),
                                qr.shape[0], scale, float(softcap), _ptr(out), _ptr(lse), _ptr(status),
                                _stream(dev))
     _check(rc, "ffa_fwd_noalloc")
@@ -376,14 +389,14 @@ def ffa_bwd(q, k, v, out, lse, dout, q_ranges, k_ranges, attn_type_map,
         _need(status, "status", torch.int32, dev)
     scale = -1.0 if softmax_scale is None else float(softmax_scale)
     if alibi_slopes is None and not deterministic:
-        rc = lib().ffa_bwd(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+        rc = _on(dev, lib().ffa_bwd, ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
                            _ptr(qr), _ptr(kr), _ptr(ty), R, scale, float(softcap), _ptr(dq), _ptr(dk),
                            _ptr(dv), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
     else:
         if alibi_slopes is not None:
             _need(alibi_slopes, "alibi_slopes", torch.float32, dev, (hq,))
         opts = FfaOptions(_ptr(alibi_slopes), 1 if deterministic else 0)
-        rc = lib().ffa_bwd_ex(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+        rc = _on(dev, lib().ffa_bwd_ex, ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
                               _ptr(qr), _ptr(kr), _ptr(ty), R, scale, float(softcap), _ptr(dq), _ptr(dk),
                               _ptr(dv), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev),
                               ctypes.byref(opts))
@@ -405,7 +418,7 @@ def ffa_plan_tiles(total_q: int, total_k: int, q_ranges, k_ranges, attn_type_map
     tc = torch.empty(max(nqt, 0), max(nkt, 0), dtype=torch.uint8, device=dev)
     f = lib().ffa_bwd_workspace_size if by_column else lib().ffa_fwd_workspace_size
     ws = torch.empty(max(int(f(ctypes.byref(shp), R)), 256), dtype=torch.uint8, device=dev)
-    rc = lib().ffa_plan_tiles(ctypes.byref(shp), _ptr(qr), _ptr(kr), _ptr(ty), R, 1 if by_column else 0,
+    rc = _on(dev, lib().ffa_plan_tiles, ctypes.byref(shp), _ptr(qr), _ptr(kr), _ptr(ty), R, 1 if by_column else 0,
                               _ptr(tc), _ptr(ws), ws.numel(), _ptr(status), _stream(dev))
     _check(rc, "ffa_plan_tiles")
     return tc

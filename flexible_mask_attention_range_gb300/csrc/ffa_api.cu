@@ -81,6 +81,14 @@ ProblemDims dims_of(const WsLayout& L) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FFA_OK : FFA_ERR_CUDA; }
 
+// Failure-detection test hook: FFA_TEST_STALL=1 makes the first wait of every CTA of the
+// next attention kernels wait on a barrier that nothing arrives on, so that the bounded wait
+// runs out (FFA_WAIT_LIMIT_NS) and the kernel takes its abort path.  Off unless set.
+int test_stall() {
+  const char* e = std::getenv("FFA_TEST_STALL");
+  return (e != nullptr && e[0] == '1' && e[1] == '\0') ? 1 : 0;
+}
+
 }  // namespace
 
 KernelEvents g_kernel_events;
@@ -112,16 +120,105 @@ bool encode_tile_map_f32(CUtensorMap* map, const void* base, uint64_t cols, uint
 }
 
 int num_sms() {
-  static int cache[64];
+  static int cache[kMaxDevices];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
   if (cache[dev] <= 0) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     cache[dev] = n > 0 ? n : 1;
   }
   return cache[dev];
+}
+
+int check_options(const ffa_options* o) {
+  if (o == nullptr) return FFA_OK;
+  for (int i = 0; i < 7; ++i)
+    if (o->reserved[i] != 0) return FFA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(o->alibi_slopes) & 3u) != 0) return FFA_ERR_INVALID_ARG;
+  return FFA_OK;
+}
+
+int fwd_check(const FwdCall& c, WsLayout* out_layout) {
+  const ffa_shape* shape = c.shape;
+  int rc = check_shape(shape, c.n_ranges);
+  if (rc != FFA_OK) return rc;
+  rc = check_options(c.options);
+  if (rc != FFA_OK) return rc;
+  if (c.paged) {
+    const int ps = c.page_size;
+    if (ps != 16 && ps != 32 && ps != 64 && ps != 128) return FFA_ERR_INVALID_ARG;
+    if (c.n_pages < 1 || c.n_pages * static_cast<int64_t>(ps) >= (static_cast<int64_t>(1) << 31))
+      return FFA_ERR_INVALID_ARG;
+    if (shape->total_k > 0 && c.page_table == nullptr) return FFA_ERR_INVALID_ARG;
+  }
+  if (std::isnan(c.softcap) || c.softcap < 0.0f) return FFA_ERR_INVALID_ARG;
+  const int64_t nq = shape->total_q, nk = shape->total_k;
+  if (nq > 0 && (c.out == nullptr || c.lse == nullptr || c.q == nullptr)) return FFA_ERR_INVALID_ARG;
+  if (nq > 0 && nk > 0 && (c.k == nullptr || c.v == nullptr)) return FFA_ERR_INVALID_ARG;
+  if (c.n_ranges > 0 && (c.q_ranges == nullptr || c.k_ranges == nullptr || c.types == nullptr))
+    return FFA_ERR_INVALID_ARG;
+  if (!aligned16(c.q) || !aligned16(c.k) || !aligned16(c.v) || !aligned16(c.out) ||
+      (reinterpret_cast<uintptr_t>(c.lse) & 3u) != 0)
+    return FFA_ERR_INVALID_ARG;
+  *out_layout = make_layout(nq, nk, shape->num_heads_q, shape->num_heads_kv, shape->head_dim, c.n_ranges);
+  return FFA_OK;
+}
+
+int fwd_launch(const FwdCall& c, const WsLayout& L, void* scratch) {
+  int rc = check_device();
+  if (rc != FFA_OK) return rc;
+  const ffa_shape* shape = c.shape;
+  const int64_t nq = shape->total_q, nk = shape->total_k;
+  cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+  const int d = shape->head_dim, hq = shape->num_heads_q;
+  if (nk == 0) {  // no key at all: every row is empty
+    if (cudaMemsetAsync(c.out, 0, static_cast<size_t>(nq) * hq * d * 2, s) != cudaSuccess) return FFA_ERR_CUDA;
+    fill_empty_fwd_kernel<<<256, 256, 0, s>>>(c.lse, static_cast<size_t>(nq) * hq);
+    return cuda_status(cudaGetLastError());
+  }
+  const ProblemDims P = dims_of(L);
+  const PlanView pv = plan_view(L, scratch);
+  cudaError_t e = launch_plan_slices(P, c.q_ranges, c.k_ranges, c.types, c.n_ranges, pv, c.status, s);
+  if (e == cudaSuccess) e = launch_plan_rows(P, L, pv, s);
+  if (e != cudaSuccess) return FFA_ERR_CUDA;
+  FwdArgs a;
+  a.P = P;
+  a.head_pair = L.head_pair ? 1 : 0;
+  a.ngrp = L.ngrp;
+  a.slots = L.slots;
+  a.n_items = L.ngrp * L.nch_max * L.slots;
+  a.split = L.split ? 1 : 0;
+  a.scale = resolve_scale(c.softmax_scale, d);
+  a.softcap = c.softcap;
+  a.q = c.q;
+  a.k = c.k;
+  a.v = c.v;
+  a.out = c.out;
+  a.lse = c.lse;
+  a.alibi = c.options != nullptr ? c.options->alibi_slopes : nullptr;
+  a.alibi_pack = c.alibi_pack;
+  if (c.paged) {
+    a.page_table = c.page_table;
+    a.page_size = c.page_size;
+    a.n_pages = c.n_pages;
+  }
+  a.plan = pv;
+  a.status = c.status;
+  a.wait_limit_ns = wait_limit_ns();
+  a.stall_test = test_stall();
+  return cuda_status(launch_fwd(a, s));
+}
+
+int fwd_with_workspace(const FwdCall& c, void* workspace, size_t workspace_bytes) {
+  WsLayout L;
+  int rc = fwd_check(c, &L);
+  if (rc != FFA_OK) return rc;
+  if (c.shape->total_q == 0) return FFA_OK;
+  if (workspace == nullptr || workspace_bytes < L.fwd_total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FFA_ERR_WORKSPACE;
+  return fwd_launch(c, L, workspace);
 }
 
 }  // namespace ffa
@@ -140,16 +237,6 @@ size_t ffa_bwd_workspace_size(const ffa_shape* s, int32_t n_ranges) {
   return make_layout(s->total_q, s->total_k, s->num_heads_q, s->num_heads_kv, s->head_dim, n_ranges).bwd_total;
 }
 
-namespace {
-int check_options(const ffa_options* o) {
-  if (o == nullptr) return FFA_OK;
-  for (int i = 0; i < 7; ++i)
-    if (o->reserved[i] != 0) return FFA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(o->alibi_slopes) & 3u) != 0) return FFA_ERR_INVALID_ARG;
-  return FFA_OK;
-}
-}  // namespace
-
 int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
             const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
             float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
@@ -158,25 +245,16 @@ int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
                     workspace, workspace_bytes, status, stream, nullptr);
 }
 
-namespace {
-struct PagedKV {
-  const int32_t* page_table = nullptr;
-  int page_size = 0;
-  int64_t n_pages = 0;
-};
-
-int fwd_common(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
-               const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
-               float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
-               void* stream, const ffa_options* options, const PagedKV& pg);
-}  // namespace
-
 int ffa_fwd_ex(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
                const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
                float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
                void* stream, const ffa_options* options) {
-  return fwd_common(shape, q, k, v, q_ranges, k_ranges, attn_type_map, n_ranges, softmax_scale, softcap, out, lse,
-                    workspace, workspace_bytes, status, stream, options, PagedKV{});
+  FwdCall c;
+  c.shape = shape; c.q = q; c.k = k; c.v = v;
+  c.q_ranges = q_ranges; c.k_ranges = k_ranges; c.types = attn_type_map; c.n_ranges = n_ranges;
+  c.softmax_scale = softmax_scale; c.softcap = softcap; c.out = out; c.lse = lse;
+  c.status = status; c.stream = stream; c.options = options;
+  return fwd_with_workspace(c, workspace, workspace_bytes);
 }
 
 int ffa_fwd_paged(const ffa_shape* shape, const void* q, const void* k_pages, const void* v_pages,
@@ -184,78 +262,15 @@ int ffa_fwd_paged(const ffa_shape* shape, const void* q, const void* k_pages, co
                   const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
                   float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
                   void* stream, const ffa_options* options) {
-  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FFA_ERR_INVALID_ARG;
-  if (n_pages < 1 || n_pages * static_cast<int64_t>(page_size) >= (static_cast<int64_t>(1) << 31))
-    return FFA_ERR_INVALID_ARG;
-  if (shape != nullptr && shape->total_k > 0 && page_table == nullptr) return FFA_ERR_INVALID_ARG;
-  PagedKV pg;
-  pg.page_table = page_table;
-  pg.page_size = page_size;
-  pg.n_pages = n_pages;
-  return fwd_common(shape, q, k_pages, v_pages, q_ranges, k_ranges, attn_type_map, n_ranges, softmax_scale, softcap,
-                    out, lse, workspace, workspace_bytes, status, stream, options, pg);
+  FwdCall c;
+  c.shape = shape; c.q = q; c.k = k_pages; c.v = v_pages;
+  c.q_ranges = q_ranges; c.k_ranges = k_ranges; c.types = attn_type_map; c.n_ranges = n_ranges;
+  c.softmax_scale = softmax_scale; c.softcap = softcap; c.out = out; c.lse = lse;
+  c.status = status; c.stream = stream; c.options = options;
+  c.page_table = page_table; c.page_size = page_size; c.n_pages = n_pages;
+  c.paged = true;
+  return fwd_with_workspace(c, workspace, workspace_bytes);
 }
-
-namespace {
-int fwd_common(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* q_ranges,
-               const int32_t* k_ranges, const int32_t* attn_type_map, int32_t n_ranges, float softmax_scale,
-               float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
-               void* stream, const ffa_options* options, const PagedKV& pg) {
-  int rc = check_shape(shape, n_ranges);
-  if (rc != FFA_OK) return rc;
-  rc = check_options(options);
-  if (rc != FFA_OK) return rc;
-  if (std::isnan(softcap) || softcap < 0.0f) return FFA_ERR_INVALID_ARG;
-  const int64_t nq = shape->total_q, nk = shape->total_k;
-  if (nq > 0 && (out == nullptr || lse == nullptr || q == nullptr)) return FFA_ERR_INVALID_ARG;
-  if (nq > 0 && nk > 0 && (k == nullptr || v == nullptr)) return FFA_ERR_INVALID_ARG;
-  if (n_ranges > 0 && (q_ranges == nullptr || k_ranges == nullptr || attn_type_map == nullptr))
-    return FFA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
-    return FFA_ERR_INVALID_ARG;
-  const WsLayout L = make_layout(nq, nk, shape->num_heads_q, shape->num_heads_kv, shape->head_dim, n_ranges);
-  if (nq == 0) return FFA_OK;
-  if (workspace == nullptr || workspace_bytes < L.fwd_total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return FFA_ERR_WORKSPACE;
-  rc = check_device();
-  if (rc != FFA_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int d = shape->head_dim, hq = shape->num_heads_q;
-  if (nk == 0) {  // no key at all: every row is empty
-    if (cudaMemsetAsync(out, 0, static_cast<size_t>(nq) * hq * d * 2, s) != cudaSuccess) return FFA_ERR_CUDA;
-    fill_empty_fwd_kernel<<<256, 256, 0, s>>>(lse, static_cast<size_t>(nq) * hq);
-    return cuda_status(cudaGetLastError());
-  }
-  const ProblemDims P = dims_of(L);
-  const PlanView pv = plan_view(L, workspace);
-  cudaError_t e = launch_plan_slices(P, q_ranges, k_ranges, attn_type_map, n_ranges, pv, status, s);
-  if (e == cudaSuccess) e = launch_plan_rows(P, L, pv, s);
-  if (e != cudaSuccess) return FFA_ERR_CUDA;
-  FwdArgs a;
-  a.P = P;
-  a.head_pair = L.head_pair ? 1 : 0;
-  a.ngrp = L.ngrp;
-  a.slots = L.slots;
-  a.n_items = L.ngrp * L.nch_max * L.slots;
-  a.split = L.split ? 1 : 0;
-  a.scale = resolve_scale(softmax_scale, d);
-  a.softcap = softcap;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.out = out;
-  a.lse = lse;
-  a.alibi = options != nullptr ? options->alibi_slopes : nullptr;
-  a.page_table = pg.page_table;
-  a.page_size = pg.page_size;
-  a.n_pages = pg.n_pages;
-  a.plan = pv;
-  a.status = status;
-  a.wait_limit_ns = wait_limit_ns();
-  return cuda_status(launch_fwd(a, s));
-}
-}  // namespace
 
 int ffa_bwd(const ffa_shape* shape, const void* q, const void* k, const void* v, const void* out,
             const float* lse, const void* dout, const int32_t* q_ranges, const int32_t* k_ranges,
@@ -336,6 +351,7 @@ int ffa_bwd_ex(const ffa_shape* shape, const void* q, const void* k, const void*
   a.plan = pv;
   a.status = status;
   a.wait_limit_ns = wait_limit_ns();
+  a.stall_test = test_stall();
   return cuda_status(launch_bwd(a, s));
 }
 

@@ -13,7 +13,8 @@
 //      query tiles of the key tile's column list and the G query heads of the group.  Five
 //      tcgen05 GEMMs per step: S^T = K Q^T and dP^T = V dO^T (keys on TMEM lanes), then
 //      dV += P^T dO and dK += dS^T Q with P^T / dS^T read from TMEM, and dQ = dS K with dS
-//      staged in shared memory; dQ is added into the fp32 accumulator with vector atomics.
+//      staged in shared memory; dQ is added into the fp32 accumulator with TMA bulk
+//      reduce-adds (cp.reduce.async.bulk.tensor, add) of 32-column boxes.
 //      dK and dV stay in TMEM for the whole item and are written once.
 //   3. ffa_bwd_dq_convert: fp32 accumulator -> bf16 dq.
 //
@@ -26,6 +27,7 @@
 // dS^T of half h over [128+64h, 128+64h+32), then dQ [128,128+D); dV [256,256+D),
 // dK [256+D,256+2D).
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
 
 #include "ffa_internal.h"
@@ -55,8 +57,8 @@ struct BwdSmem {
   static constexpr int kStat = kDS + kTile * kTile * 2;            // + s * kStatBytes
   static constexpr int kBar = kStat + kStages * kStatBytes;
   // kv_full, kv_empty, qdo_full[S], qdo_empty[S], s_full, dp_full, p_full, ds_full, dq_full,
-  // dq_empty, dkv_full, drain, sds_free
-  static constexpr int kNumBars = 2 + 2 * kStages + 9;
+  // dq_empty, dkv_full, drain, sds_free, stall (never arrived on; failure-detection test)
+  static constexpr int kNumBars = 2 + 2 * kStages + 10;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kMaxDyn = 232448;
@@ -84,6 +86,7 @@ struct BwdParams {
   int* dq_sem;
   int* status;
   uint64_t wait_limit_ns;
+  int stall;  // failure-detection test: the first wait of every CTA never completes
 };
 
 __device__ __forceinline__ int sched_item(int wave) {
@@ -252,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dkv_full = s_full + 6;
   uint64_t* drain = s_full + 7;
   uint64_t* sds_free = s_full + 8;
+  uint64_t* stall_bar = s_full + 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM::kMisc + 4);
 
@@ -272,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dkv_full, 1);
     mbar_init(drain, 1);
     mbar_init(sds_free, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -327,8 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = step_cnt % S;
         const float* stat = reinterpret_cast<const float*>(sm + SM::kStat + st * SM::kStatBytes);
         // the row statistics arrive with the stage's Q/dO (qdo_full); S^T with s_full
+        uint64_t* sb = (p.stall && step_cnt == 0) ? stall_bar : s_full;
         ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (step_cnt / S) & 1u, abort_flag, lim) &&
-                                         mbar_wait(s_full, step_cnt & 1u, abort_flag, lim));
+                                         mbar_wait(sb, step_cnt & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
         uint32_t w[4];
@@ -809,13 +815,16 @@ __global__ void __launch_bounds__(256) ffa_bwd_dq_convert(const float* __restric
 template <int D, bool kCap, bool kBias, bool kDet>
 cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   using SM = BwdSmem<D>;
-  static bool attr_set = false;
   auto kern = ffa_bwd_kernel<D, kCap, kBias, kDet>;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // once per device: the shared-memory attribute applies to the device current when it is set
+  static std::once_flag once[kMaxDevices];
+  static cudaError_t setup_err[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    setup_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+  });
+  if (setup_err[dev] != cudaSuccess) return setup_err[dev];
   const auto& P = a.P;
   const int qpad = P.nqt * kTile;
   const int nsm = num_sms();
@@ -858,6 +867,7 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   p.dq_sem = a.dq_sem;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
+  p.stall = a.stall_test;
   const int grid = p.n_items < nsm ? p.n_items : nsm;
   if (grid > 0) {
     if (g_kernel_events.bwd_start != nullptr) cudaEventRecord(g_kernel_events.bwd_start, stream);

@@ -20,8 +20,10 @@
 // slices, one per token i, over the keys that token sees under the bottom-right alignment
 // used everywhere in this library (j <= i + ke - qe).  max_seqlen_q bounds m, so the
 // rewritten list has a fixed length n_ranges * max_seqlen_q (unused entries are empty
-// slices).  Packing, rewriting and unpacking are three small kernels around ffa_fwd_ex /
-// ffa_fwd_paged.
+// slices).  Packing, rewriting and unpacking are three small kernels around the forward pass
+// (dense or paged).  With ALiBi (FlexAttention paper, sections 2 and 3.1; decoding with GQA
+// and ALiBi is one of the cases its section 6 measures) a packed row keeps the slope of its
+// query head and the position of its token, so the bias is the one of the unpacked problem.
 #include <cstdint>
 
 #include "../../include/ffa.h"
@@ -163,7 +165,7 @@ int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const v
                    float softcap, void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
                    void* stream, const ffa_options* options) {
   if (shape == nullptr || n_ranges < 0 || max_seqlen_q < 1) return FFA_ERR_INVALID_ARG;
-  if (options != nullptr && options->alibi_slopes != nullptr) return FFA_ERR_UNSUPPORTED;
+  if (check_options(options) != FFA_OK) return FFA_ERR_INVALID_ARG;
   if (shape->head_dim != 64 && shape->head_dim != 128) return FFA_ERR_UNSUPPORTED;
   if (shape->num_heads_kv < 1 || shape->num_heads_q < 1 || shape->num_heads_q % shape->num_heads_kv != 0)
     return FFA_ERR_INVALID_ARG;
@@ -198,17 +200,21 @@ int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const v
                                      shape->total_k, qr2, kr2, ty2, status);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
-  const size_t inner_bytes = workspace_bytes - L.inner;
-  int rc;
-  if (page_table == nullptr) {
-    rc = ffa_fwd_ex(&L.inner_shape, wb + L.qp, k, v, qr2, kr2, ty2, static_cast<int32_t>(L.R2), softmax_scale, softcap,
-                    wb + L.op, reinterpret_cast<float*>(wb + L.lsep), wb + L.inner, inner_bytes, status, stream,
-                    options);
-  } else {
-    rc = ffa_fwd_paged(&L.inner_shape, wb + L.qp, k, v, page_table, page_size, n_pages, qr2, kr2, ty2,
-                       static_cast<int32_t>(L.R2), softmax_scale, softcap, wb + L.op,
-                       reinterpret_cast<float*>(wb + L.lsep), wb + L.inner, inner_bytes, status, stream, options);
+  // the forward pass over the packed problem; with ALiBi each packed row takes the slope of
+  // its query head and the position of its token (FwdArgs::alibi_pack)
+  FwdCall c;
+  c.shape = &L.inner_shape;
+  c.q = wb + L.qp; c.k = k; c.v = v;
+  c.q_ranges = qr2; c.k_ranges = kr2; c.types = ty2; c.n_ranges = static_cast<int32_t>(L.R2);
+  c.softmax_scale = softmax_scale; c.softcap = softcap;
+  c.out = wb + L.op; c.lse = reinterpret_cast<float*>(wb + L.lsep);
+  c.status = status; c.stream = stream; c.options = options;
+  c.alibi_pack = P;
+  if (page_table != nullptr) {
+    c.paged = true;
+    c.page_table = page_table; c.page_size = page_size; c.n_pages = n_pages;
   }
+  const int rc = fwd_with_workspace(c, wb + L.inner, workspace_bytes - L.inner);
   if (rc != FFA_OK) return rc;
   decode_unpack<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(wb + L.op), static_cast<uint4*>(out),
                                        reinterpret_cast<const float*>(wb + L.lsep), lse, nq, hq, P, d);

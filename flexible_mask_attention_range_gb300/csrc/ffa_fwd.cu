@@ -37,6 +37,7 @@
 // only then is that row of O rescaled in TMEM.  Rows with no visible key so far use 0 as
 // the reference (safe softmax), so fully masked rows end with l = 0: O = 0, LSE = -inf.
 #include <cmath>
+#include <mutex>
 #include <type_traits>
 
 #include "ffa_internal.h"
@@ -66,8 +67,9 @@ struct FwdSmem {
   static constexpr int kK = 2 * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kBar = kV + kStages * kTileBytes;
-  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain
-  static constexpr int kNumBars = 2 + 3 * kStages + 7;
+  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain,
+  // stall (never arrived on; the failure-detection test waits on it)
+  static constexpr int kNumBars = 2 + 3 * kStages + 8;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;
@@ -87,10 +89,12 @@ struct FwdParams {
   __nv_bfloat16* out;
   float* lse;
   const float* alibi;  // per-query-head ALiBi slopes, or null
+  int alibi_pack;      // > 0: packed decode rows (slope of head h*pack + r%pack, position r/pack)
   const int32_t* page_table;  // paged K/V: physical page of each logical page, else null
   int page_size, n_lpages, n_pages;
   int* status;
   uint64_t wait_limit_ns;
+  int stall;  // failure-detection test: the first wait of every CTA never completes
 };
 
 struct Item {
@@ -257,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_full = s_full + 4;
   uint64_t* drain = s_full + 6;
+  uint64_t* stall_bar = s_full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM::kMisc + 4);
 
@@ -275,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_full[t], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -323,7 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const uint32_t* ents = it.ents;
-      const float slope_log2 = kBias ? p.alibi[h] * kLog2e : 0.0f;
+      // ALiBi slope and query position of this row (packed decode rows: the row's own query
+      // head and token)
+      int a_head = h, a_pos = row;
+      if (kBias && p.alibi_pack > 0) {
+        a_head = h * p.alibi_pack + row % p.alibi_pack;
+        a_pos = row / p.alibi_pack;
+      }
+      const float slope_log2 = kBias ? p.alibi[a_head] * kLog2e : 0.0f;
       const int nsl = qt < p.nqt ? p.plan.row_nsl[qt] : 0;
       const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
       // this row's visible keys once per item; PARTIAL tiles clip them instead of rereading
@@ -340,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + 1 < n) e_next = ents[j + 1];  // in flight while this tile is processed
         const int kt = entry_idx(e);
         const int cls = entry_cls(e, wg);
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], s_cnt & 1u, abort_flag, lim));
+        uint64_t* sb = (p.stall && s_cnt == 0) ? stall_bar : &s_full[wg];
+        ok = __all_sync(0xffffffffu, mbar_wait(sb, s_cnt & 1u, abort_flag, lim));
         if (!ok) break;
         ++s_cnt;
         tc_fence_after();
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) reg_fence(sv[c]);
         const bool masked = (cls != FFA_TILE_FULL) || (kt * kTile + kTile > p.nk);
         // ALiBi in the log2 domain: slope * log2(e) * (key - row) = bbase + slope * log2(e) * c
-        const float bbase = kBias ? slope_log2 * static_cast<float>(kt * kTile - row) : 0.0f;
+        const float bbase = kBias ? slope_log2 * static_cast<float>(kt * kTile - a_pos) : 0.0f;
         // Softcap on a fully visible tile: when every raw score of the warp's rows lies where
         // the tanh polynomial holds, the logits are formed inside the exponential pass (FMA
         // pipe only), and the row max is the polynomial at the raw max, the transform being
@@ -789,20 +803,23 @@ __global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
 template <int D, bool kCap, bool kBias>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   using SM = FwdSmem<D>;
-  static bool attr_set = false;
   auto kern = ffa_fwd_kernel<D, kCap, kBias>;
-  if (!attr_set) {
-    // The register split (setmaxnreg) is balanced for exactly kRegsLaunch registers per
-    // thread at launch; with any other count a softmax warp's increase could never be
-    // granted, so such a build is refused here rather than launched.
+  // Once per device (the shared-memory attribute applies to the device current when it is
+  // set).  The register split (setmaxnreg) is balanced for exactly kRegsLaunch registers per
+  // thread at launch; with any other count a softmax warp's increase could never be granted,
+  // so such a build is refused here rather than launched.
+  static std::once_flag once[kMaxDevices];
+  static cudaError_t setup_err[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    if (e == cudaSuccess && fa.numRegs != kRegsLaunch) e = cudaErrorInvalidKernelImage;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+    setup_err[dev] = e;
+  });
+  if (setup_err[dev] != cudaSuccess) return setup_err[dev];
   CUtensorMap mq, mk, mv;
   const auto& P = a.P;
   // paged: K/V maps cover the physical pool, one page of rows per box
@@ -825,12 +842,14 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.alibi = a.alibi;
+  p.alibi_pack = a.alibi_pack;
   p.page_table = a.page_table;
   p.page_size = paged ? a.page_size : 0;
   p.n_pages = paged ? static_cast<int>(a.n_pages) : 0;
   p.n_lpages = paged ? static_cast<int>((static_cast<int64_t>(P.nk) + a.page_size - 1) / a.page_size) : 0;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
+  p.stall = a.stall_test;
   const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
   if (grid <= 0) return cudaSuccess;
   if (g_kernel_events.fwd_start != nullptr) cudaEventRecord(g_kernel_events.fwd_start, stream);

@@ -8,12 +8,15 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "../../include/ffa.h"
+
 namespace ffa {
 
 constexpr int kTile = 128;         // global tile edge (query rows and key columns)
 constexpr int kSliceCap = 64;      // slice ids stored per tile row / tile column for masks
 constexpr int kSliceSmem = 512;    // slices staged in shared memory by the planner
 constexpr int kMaxTiles = 8192;    // ceil(FFA_MAX_TOKENS / 128)
+constexpr int kMaxDevices = 64;    // per-device caches (function attributes, SM counts, scratch)
 // Forward work lists are cut into chunks when there are too few work items to fill the GPU:
 // the planner then aims at about kSplitTarget chunks (two per SM on a 152-SM part) of at least
 // kMinChunk key tiles, and a merge kernel combines the chunks' partial results by LSE.
@@ -50,12 +53,12 @@ struct WsLayout {
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Softcap as a polynomial: tanh(y) / y ~ c0 + c1 y^2 + c2 y^4 + c3 y^6 on |y| <= kTanhPolyY.
-// The coefficients were fitted in float64 for minimax relative error (least squares on
-// Chebyshev nodes, reweighted by the error until it equioscillates); evaluated by Horner's
-// rule in float32 the product y * P(y^2) stays within 1.6e-7 of tanh(y), relative, over the
-// whole interval.
+// The coefficients are the output of fit_tanh_poly.py (next to this package's build script):
+// a float64 minimax fit of the relative error (least squares on Chebyshev nodes, reweighted
+// by the error until it equioscillates).  Evaluated by Horner's rule in float32, the product
+// y * P(y^2) stays within 1.6e-7 of tanh(y), relative, over the whole interval.
 constexpr double kTanhPolyY = 0.375;
-constexpr double kTanhPoly[4] = {9.999999421e-01, -3.333199304e-01, 1.328484108e-01, -4.828819503e-02};
+constexpr double kTanhPoly[4] = {9.999999405e-01, -3.333197486e-01, 1.328450275e-01, -4.827228855e-02};
 
 // The capped logit in the log2 domain, x(s) = C tanh(a s) with a = scale / softcap and
 // C = softcap * log2(e), folded into one odd polynomial of the raw score:
@@ -215,6 +218,10 @@ struct FwdArgs {
   void* out;
   float* lse;
   const float* alibi = nullptr;  // per-query-head ALiBi slopes (device) or null
+  // alibi_pack > 0 (decode): row r of query head h is token r / alibi_pack of the caller's
+  // query head h * alibi_pack + r % alibi_pack; the bias uses that head's slope and that
+  // token's position.
+  int alibi_pack = 0;
   // Paged K/V (page_size > 0): k and v are physical page pools [n_pages * page_size, Hkv, d];
   // logical page j of the key sequence lives in physical page page_table[j].
   const int32_t* page_table = nullptr;
@@ -223,6 +230,7 @@ struct FwdArgs {
   PlanView plan;
   int32_t* status;
   uint64_t wait_limit_ns;
+  int stall_test = 0;  // failure-detection test hook (FFA_TEST_STALL)
 };
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 
@@ -243,8 +251,38 @@ struct BwdArgs {
   PlanView plan;
   int32_t* status;
   uint64_t wait_limit_ns;
+  int stall_test = 0;  // failure-detection test hook (FFA_TEST_STALL)
 };
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
+
+// The forward entry points' arguments (ffa_api.cu).  ffa_fwd_ex, ffa_fwd_paged, ffa_fwd_decode
+// and ffa_fwd_noalloc fill one and share the checks and the launch sequence.
+struct FwdCall {
+  const ffa_shape* shape = nullptr;
+  const void *q = nullptr, *k = nullptr, *v = nullptr;
+  const int32_t *q_ranges = nullptr, *k_ranges = nullptr, *types = nullptr;
+  int32_t n_ranges = 0;
+  float softmax_scale = 0.0f, softcap = 0.0f;
+  void* out = nullptr;
+  float* lse = nullptr;
+  int32_t* status = nullptr;
+  void* stream = nullptr;
+  const ffa_options* options = nullptr;
+  bool paged = false;  // k, v are page pools reached through page_table
+  const int32_t* page_table = nullptr;
+  int page_size = 0;
+  int64_t n_pages = 0;
+  int alibi_pack = 0;  // > 0: rows are packed (token, query head) pairs (decode), see FwdArgs
+};
+// Options check shared by the entry points: reserved fields zero, slopes 4-byte aligned.
+int check_options(const ffa_options* o);
+// Host-detectable errors of a forward call (nothing is launched); fills the workspace layout.
+int fwd_check(const FwdCall& c, WsLayout* layout);
+// Device check, planner and kernels, with the planner's scratch at `scratch` (at least
+// layout.fwd_total bytes, 256-byte aligned).  total_q must be > 0.
+int fwd_launch(const FwdCall& c, const WsLayout& layout, void* scratch);
+// fwd_check, then fwd_launch on a caller workspace.
+int fwd_with_workspace(const FwdCall& c, void* workspace, size_t workspace_bytes);
 
 // Optional events recorded around the main kernels (ffa_api.cu)
 struct KernelEvents {

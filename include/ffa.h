@@ -36,6 +36,12 @@
  *     bounded wait inside a kernel that runs out ORs FFA_STATUS_TIMEOUT into *status.
  *     *status is a device int32 that the library only ORs into (the caller clears it);
  *     it may be NULL.
+ *   - Environment, read on every call: FFA_WAIT_LIMIT_NS (decimal) bounds every wait inside
+ *     a kernel (default 4 s).  FFA_TEST_STALL=1 is a failure-detection test switch: the first
+ *     wait of every CTA of the forward and backward attention kernels then targets a barrier
+ *     that nothing arrives on, so it runs out after FFA_WAIT_LIMIT_NS, the kernel records
+ *     FFA_STATUS_TIMEOUT, lets its in-flight copies and MMAs land, frees its tensor memory and
+ *     returns (outputs are then undefined).  Leave it unset in normal use.
  */
 #ifndef FFA_H_
 #define FFA_H_
@@ -94,7 +100,11 @@ size_t ffa_fwd_workspace_size(const ffa_shape* shape, int32_t n_ranges);
 size_t ffa_bwd_workspace_size(const ffa_shape* shape, int32_t n_ranges);
 
 /*
- * Forward pass: out, lse = attention(q, k, v, slices).
+ * Forward pass: out, lse = attention(q, k, v, slices).  This is flex_flash_attn_func(q, k, v,
+ * max_seqlen_q, max_seqlen_k, q_ranges, k_ranges, attn_type_map, softmax_scale, softcap) ->
+ * (out, lse) of MagiAttention issue #180 (the reproduction script's attention call); the
+ * max_seqlen arguments are not needed because tiles lie on the global grid of the packed
+ * tensors.
  *   q        device bf16 [Nq, Hq, d]
  *   k, v     device bf16 [Nk, Hkv, d]
  *   q_ranges, k_ranges  device int32 [n_ranges, 2] (start, end) pairs, end exclusive
@@ -116,7 +126,8 @@ int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
             void* stream);
 
 /*
- * Backward pass: gradients of sum(out * dout) with respect to q, k and v.
+ * Backward pass: gradients of sum(out * dout) with respect to q, k and v, the dq/dk/dv that
+ * MagiAttention issue #180's reproduction script obtains with out.backward(do).
  *   q, k, v, q_ranges, k_ranges, attn_type_map, n_ranges, softmax_scale, softcap: as for
  *            ffa_fwd (same values as the forward call)
  *   out      device bf16 [Nq, Hq, d]: the forward output
@@ -125,8 +136,9 @@ int ffa_fwd(const ffa_shape* shape, const void* q, const void* k, const void* v,
  *   dq       device bf16 [Nq, Hq, d], written
  *   dk, dv   device bf16 [Nk, Hkv, d], written
  *   workspace  at least ffa_bwd_workspace_size() bytes
- * dq is accumulated in float32 with atomic adds, so it may differ in the last bits from
- * run to run; dk and dv are written once per (key tile, kv head).
+ * dq is accumulated in a float32 buffer by TMA bulk reduce-adds from many CTAs, so its
+ * summation order (and its last bits) may differ from run to run; dk and dv are written once
+ * per (key tile, kv head).  ffa_bwd_ex with deterministic = 1 fixes the order.
  */
 int ffa_bwd(const ffa_shape* shape, const void* q, const void* k, const void* v, const void* out,
             const float* lse, const void* dout, const int32_t* q_ranges, const int32_t* k_ranges,
@@ -202,8 +214,10 @@ int ffa_fwd_paged(const ffa_shape* shape, const void* q, const void* k_pages, co
  *                 reported with FFA_STATUS_BAD_RANGE
  * The query heads of every token are processed as rows of the key/value head they share
  * (G / 2 rows per packed head when G = Hq / Hkv is even, G otherwise), so each key tile is
- * read once per key/value head instead of once per pair of query heads.  ALiBi is not available here (FFA_ERR_UNSUPPORTED).  Requires
- * total_q * G <= FFA_MAX_TOKENS.  workspace: ffa_fwd_decode_workspace_size() bytes.
+ * read once per key/value head instead of once per pair of query heads.  options->alibi_slopes
+ * ([Hq], as for ffa_fwd_ex) gives every query head its own slope and every token its own
+ * position, exactly as in the unpacked problem.  Requires total_q * G <= FFA_MAX_TOKENS.
+ * workspace: ffa_fwd_decode_workspace_size() bytes.
  */
 size_t ffa_fwd_decode_workspace_size(const ffa_shape* shape, int32_t n_ranges, int32_t max_seqlen_q);
 int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const void* v, const int32_t* page_table,

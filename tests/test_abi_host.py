@@ -110,8 +110,9 @@ def test_decode_argument_checks(lib_path):
 
     assert call(max_q=0) == 1
     assert call(shape=ffa.FfaShape(16, 4096, 8, 2, 96)) == 2                # head_dim
-    slopes = ffa.FfaOptions(16)
-    assert call(opts=ctypes.byref(slopes)) == 2                             # ALiBi not here
+    assert call(opts=ctypes.byref(ffa.FfaOptions(18))) == 1                 # misaligned slopes
+    assert call(opts=ctypes.byref(ffa.FfaOptions(16, 0, (ctypes.c_int32 * 7)(1)))) == 1   # reserved
+    assert call(opts=ctypes.byref(ffa.FfaOptions(16))) == 4                 # ALiBi accepted
     assert call() == 4                                                      # then: no workspace
 
 

@@ -125,3 +125,56 @@ def test_decode_softcap_and_odd_groups(hq, hkv, cap):
     ro, rl = O.forward(q, k, v, qr, kr, ty, softmax_scale=scale, softcap=cap)
     assert_out_close(to64(o), ro)
     assert_lse_close(to64(l), rl)
+
+
+# Decoding with GQA and ALiBi (FlexAttention paper, section 6, "Inference Performance": the
+# decoding case it singles out): every query head keeps its own slope and every token its
+# own position after the heads are packed as rows.
+DECODE_ALIBI = [
+    # n_seq, q_len, hq, hkv, d, cap, paged, seed
+    (24, 1, 16, 4, 128, 0.0, False, 61),    # G = 4: two packed heads of 2 rows per KV head
+    (10, 3, 32, 4, 128, 30.0, False, 62),   # G = 8, several new tokens (CAUSAL rewrite)
+    (8, 2, 16, 2, 64, 0.0, True, 63),       # G = 8, paged cache
+    (6, 2, 12, 4, 128, 5.0, True, 64),      # G = 3 (odd: all heads packed), paged
+]
+
+
+@pytest.mark.parametrize("n_seq,q_len,hq,hkv,d,cap,paged,seed", DECODE_ALIBI)
+def test_decode_alibi(n_seq, q_len, hq, hkv, d, cap, paged, seed):
+    qr, kr, ty, nq, nk = _batch(n_seq, q_len, seed, 150, 2500)
+    g = W.make_generator(seed + 100)
+    q = torch.randn(nq, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(nk, hkv, d, generator=g).to(torch.bfloat16)
+    # Positions are packed token indices, so the queries of a decode batch sit far from their
+    # keys; only the bias differences between the keys of one sequence (up to 2500 apart)
+    # shape a row's softmax.  Slopes 2^-6 .. 2^-12 keep those differences between about 40
+    # and 0.6 logits: sharp for some heads, flat for others, so a slope taken from the wrong
+    # head shows.
+    slopes = [2.0 ** (-6.0 - 6.0 * h / (hq - 1)) for h in range(hq)]
+    al = torch.tensor(slopes, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if paged:
+        page = 32
+        n_lp = math.ceil(nk / page)
+        table = W.random_page_table(n_lp, n_lp + 3, seed + 200)
+        kp = torch.zeros(n_lp + 3, page, hkv, d, dtype=torch.bfloat16)
+        vp = torch.zeros(n_lp + 3, page, hkv, d, dtype=torch.bfloat16)
+        for j in range(n_lp):
+            rows = min(page, nk - j * page)
+            kp[int(table[j]), :rows] = k[j * page:j * page + rows]
+            vp[int(table[j]), :rows] = v[j * page:j * page + rows]
+        o, l = ffa.ffa_fwd_decode(q.cuda(), kp.cuda(), vp.cuda(), qr, kr, ty, max_seqlen_q=q_len, softcap=cap,
+                                  page_table=table.cuda(), total_k=nk, status=status, alibi_slopes=al)
+    else:
+        o, l = ffa.ffa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, max_seqlen_q=q_len, softcap=cap,
+                                  status=status, alibi_slopes=al)
+    o_f, l_f = ffa.ffa_fwd(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, softcap=cap, alibi_slopes=al)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ro, rl = O.forward(q, k, v, qr, kr, ty, softcap=cap, alibi_slopes=slopes)
+    assert_out_close(to64(o), ro)
+    assert_lse_close(to64(l), rl)
+    # the token-major forward pass with the same slopes agrees up to summation order
+    assert (o.float() - o_f.float()).abs().max().item() <= 2e-2
+    assert (l - l_f).abs().max().item() <= 1e-3

@@ -82,9 +82,11 @@ RANDOM = [
 def test_random_slices(nq, nk, hq, hkv, d, R, cap, seed):
     q, k, v, _ = _draw2(nq, nk, hq, hkv, d, seed)
     qr, kr, ty = W.random_slices(nq, nk, R, seed=seed)
-    # explicit scales stay in the workloads' logit regime (about 1/sqrt(d)); a scale several
-    # times larger makes |dq| ~ 10, where bf16 storage alone approaches the 5e-2 bound
-    scale = None if seed % 2 else 0.75 / d ** 0.5
+    # even seeds take an explicit, sharp scale (logit standard deviation 8 at d = 64 and 3.4
+    # at d = 128): rows are dominated by a few keys and the lazily moved reference max is
+    # often stale.  O is a convex combination of bf16 values of V, so its bf16 rounding stays
+    # far inside the bound however sharp the softmax is.
+    scale = None if seed % 2 else (1.0 if d == 64 else 0.3)
     _check_full(q, k, v, qr, kr, ty, scale, cap)
 
 

@@ -71,3 +71,12 @@ def test_folded_form_in_the_raw_score():
         ref = C * np.tanh(a * s.astype(np.float64))
         # absolute error of the log2-domain logit: a relative error of p of about 1e-6
         assert np.abs(x - ref).max() < 1e-6 * max(1.0, C * math.tanh(y0))
+
+
+def test_header_coefficients_are_the_generator_output():
+    """The constants in the header are what the committed fitting script produces."""
+    from flexible_mask_attention_range_gb300 import fit_tanh_poly as F
+    y0, c = _constants()
+    assert y0 == F.Y
+    fitted = F.fit()
+    assert [f"{x:.9e}" for x in fitted] == [f"{x:.9e}" for x in c]
