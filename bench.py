@@ -377,6 +377,52 @@ def algorithmic_bytes(w: W.Workload):
     return fwd, bwd
 
 
+def time_calls(w: W.Workload, calls: int, phase: str):
+    """`calls` forward and/or backward calls of one workload, each timed with CUDA events
+    (whole call and main kernel), L2 flushed before each; a fixed launch sequence for
+    profilers (ncu -s / -c count the main-kernel launches of these calls)."""
+    import flexible_mask_attention_range_gb300 as ffa
+    from flexible_mask_attention_range_gb300 import build as ffa_build
+    ffa_build.ensure_built()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    q_h, k_h, v_h, do_h, qr_h, kr_h, ty_h = make_inputs(w)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    qr, kr, ty = (t.to(dev) for t in (qr_h, kr_h, ty_h))
+    out = torch.empty_like(q)
+    lse = torch.empty(w.hq, w.total, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    do_fwd = phase in ("fwd", "both") or not w.backward
+    do_bwd = phase in ("bwd", "both") and w.backward
+    t = {"fwd": [], "bwd": []}
+    if not do_fwd:  # the backward needs out and lse
+        ffa.ffa_fwd(q, k, v, qr, kr, ty, w.softmax_scale, w.softcap, out=out, lse=lse, status=st)
+    for _ in range(calls):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        if do_fwd:
+            flush.zero_()
+            ev[0].record()
+            ffa.ffa_fwd(q, k, v, qr, kr, ty, w.softmax_scale, w.softcap, out=out, lse=lse, status=st)
+            ev[1].record()
+        if do_bwd:
+            flush.zero_()
+            ev[2].record()
+            ffa.ffa_bwd(q, k, v, out, lse, do, qr, kr, ty, w.softmax_scale, w.softcap, dq=dq, dk=dk, dv=dv,
+                        status=st)
+            ev[3].record()
+        torch.cuda.synchronize()
+        if do_fwd:
+            t["fwd"].append(ev[0].elapsed_time(ev[1]))
+        if do_bwd:
+            t["bwd"].append(ev[2].elapsed_time(ev[3]))
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    return {"workload": w.name, "calls": calls,
+            **{f"{ph}_ms_median": round(statistics.median(x), 4) for ph, x in t.items() if x}}
+
+
 def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
     """Every workload of the project timed alone on this GPU: the whole forward call (planner,
     kernel, merge) and backward call (planner, preprocess, kernel, dq conversion) with CUDA
@@ -459,10 +505,10 @@ def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
 # source changes the figure no longer describes the kernel, and `traffic` is reported null.
 TRAFFIC = {
     # (workload, kernel): (bytes per launch, source hash at capture)
-    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1827558912 + 234647296, "629d7a67262ba57b"),
-    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (12691239168 + 6128407296, "f3a33f7eda8f2c7b"),
-    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541525760 + 237864192, "629d7a67262ba57b"),
-    ("sliding_32k_softcap", "ffa_bwd_kernel"): (6673673984 + 3498322176, "f3a33f7eda8f2c7b"),
+    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1810359552 + 234913792, "10bfa9534f737a60"),
+    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (12508939008 + 5972337408, "f3a33f7eda8f2c7b"),
+    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541674240 + 236363008, "10bfa9534f737a60"),
+    ("sliding_32k_softcap", "ffa_bwd_kernel"): (6672052480 + 3488093184, "f3a33f7eda8f2c7b"),
 }
 
 
@@ -609,6 +655,9 @@ def main():
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload table")
     ap.add_argument("--oracle-report", action="store_true",
                     help="time the float64 oracle on the host cores for every workload and exit")
+    ap.add_argument("--calls", type=int, default=0,
+                    help="time N forward (and backward) calls of --workload alone and exit (profiling aid)")
+    ap.add_argument("--phase", choices=["fwd", "bwd", "both"], default="both")
     ap.add_argument("--oracle-configs", default=",".join(W.ORDER))
     ap.add_argument("--oracle-single", default="tiny_256,page1_2048_gqa,docs_16k",
                     help="workloads also timed on one BLAS thread (empty: none)")
@@ -621,6 +670,9 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     w = W.get(args.workload)
+    if args.calls > 0:
+        print(json.dumps(time_calls(w, args.calls, args.phase)), flush=True)
+        return
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         if rank == 0:

@@ -85,6 +85,10 @@ struct FwdParams {
   // x = s * (q0 + q1 s^2 + q2 s^4 + q3 s^6), valid for |s| <= cap_slim (< 0: never used)
   float cap_q[4];
   float cap_slim;
+  // softcap bounds every logit to (-cap_c, cap_c) (log2 domain); when 2 * cap_c <= 120 the
+  // exponentials of the softcap kernel use the fixed reference cap_c: 2^(x - cap_c) lies in
+  // (2^-120, 1], so nothing overflows or flushes to zero and no row max or rescale is needed
+  int cap_fixed;
   PlanView plan;
   __nv_bfloat16* out;
   float* lse;
@@ -176,6 +180,29 @@ __device__ __forceinline__ void row_mask(const FwdParams& p, int cls, int row, i
   }
 }
 
+// Element mask of query row `row` over key tile kt from the row's visible intervals (when the
+// union of its slices has at most two) or from the slice list.
+__device__ __forceinline__ void tile_mask(const FwdParams& p, int cls, int row, int kt, int nsl, const int* sl,
+                                          bool ivl_ok, int ilo0, int ihi0, int ilo1, int ihi1, uint32_t (&w)[4]) {
+  if (ivl_ok && cls != FFA_TILE_FULL) {
+    const int c0 = kt * kTile;
+    w[0] = w[1] = w[2] = w[3] = 0u;
+    if (cls == FFA_TILE_PARTIAL) {
+      set_bits(w, max(ilo0 - c0, 0), min(ihi0 - c0, kTile));
+      set_bits(w, max(ilo1 - c0, 0), min(ihi1 - c0, kTile));
+    }
+    const int valid = p.nk - c0;
+    if (valid < kTile) {
+      uint32_t t4[4] = {0u, 0u, 0u, 0u};
+      set_bits(t4, 0, valid);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[k] &= t4[k];
+    }
+  } else {
+    row_mask(p, cls, row, kt, nsl, sl, w);
+  }
+}
+
 // The keys visible to query row `row` as at most two disjoint intervals (the union of the
 // row's slices, merged).  Returns false when the union needs more than two intervals.
 __device__ __forceinline__ bool row_intervals(const FwdParams& p, int row, int nsl, const int* sl, int& lo0,
@@ -241,7 +268,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint3
   }
 }
 
-template <int D, bool kCap, bool kBias>
+// kFixed: bounded softcap (kCap, no bias, 2 * cap_c <= 120): fixed reference max cap_c
+template <int D, bool kCap, bool kBias, bool kFixed>
 __global__ void __launch_bounds__(kThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -346,8 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t e_next = ents[0];
       // l_run: sum of the fp32 p (for the LSE); r_run: sum of the bf16-rounded p that the PV
       // MMA actually multiplies (normalising O by it keeps the weights a convex combination,
-      // so a dominant key is reproduced exactly even when the reference max is stale)
-      float m_run = -INFINITY, l_run = 0.0f, r_run = 0.0f;
+      // so a dominant key is reproduced exactly even when the reference max is stale).  On
+      // tiles without ALiBi and without a mask r_run takes the fp32 sum plus the rounding error
+      // of the tile's largest p only: that is the term that matters when one key dominates,
+      // at a fraction of the cost of rounding every p back
+      // m_run: the reference max of the exponentials (log2 domain); a bounded softcap fixes it
+      float m_run = kFixed ? p.cap_c : -INFINITY, l_run = 0.0f, r_run = 0.0f;
       for (int j = 0; j < n; ++j) {
         const uint32_t e = e_next;
         if (j + 1 < n) e_next = ents[j + 1];  // in flight while this tile is processed
@@ -365,16 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence(sv[c]);
         const bool masked = (cls != FFA_TILE_FULL) || (kt * kTile + kTile > p.nk);
-        // ALiBi in the log2 domain: slope * log2(e) * (key - row) = bbase + slope * log2(e) * c
-        const float bbase = kBias ? slope_log2 * static_cast<float>(kt * kTile - a_pos) : 0.0f;
-        // Softcap on a fully visible tile: when every raw score of the warp's rows lies where
-        // the tanh polynomial holds, the logits are formed inside the exponential pass (FMA
-        // pipe only), and the row max is the polynomial at the raw max, the transform being
-        // increasing there.  Otherwise (and on masked tiles) the exact transform runs first.
-        constexpr bool kPolyCap = kCap && !kBias;
-        bool poly = false;
-        float mx = -INFINITY;
-        if (kPolyCap && !masked) {
+        bool rescale = false;  // the reference max moved: O rows are scaled by alpha
+        float alpha = 1.0f;
+        if constexpr (kFixed) {
+          // Bounded softcap: every capped logit lies in (-cap_c, cap_c), so the exponentials
+          // use the fixed reference m_run = cap_c and no row max is taken.  The tanh
+          // polynomial forms the logits inside the exponential pass when every raw score of
+          // the warp's rows lies where it holds (tanh is odd: a bound on |s|); otherwise the
+          // exact transform runs first.  Masked entries are set to -inf after the transform.
           float hi[4], lo[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -389,118 +419,215 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float smax = fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3]));
           const float smin = fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3]));
-          poly = __all_sync(0xffffffffu, fmaxf(smax, -smin) <= p.cap_slim);
-          if (poly) {
-            const float t = smax * smax;
-            mx = smax * fmaf(fmaf(fmaf(p.cap_q[3], t, p.cap_q[2]), t, p.cap_q[1]), t, p.cap_q[0]);
+          const bool poly_f = __all_sync(0xffffffffu, fmaxf(smax, -smin) <= p.cap_slim);
+          if (!poly_f) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              sv[c >> 5][c & 31] =
+                  __float_as_uint(capped_log2(__uint_as_float(sv[c >> 5][c & 31]), p.cap_c, p.cap_k));
           }
-        }
-        // row max: eight independent partial maxima when the logits are formed first (a
-        // longer transform per element), one chain otherwise (measured faster there)
-        constexpr int kMx = kPre ? 8 : 1;
-        float mxs[kMx];
+          uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+          if (masked) tile_mask(p, cls, row, kt, nsl, sl, ivl_ok, ilo0, ihi0, ilo1, ihi1, w);
+          float2 sum2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+          float2 sumr2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+          const float2 nm2 = make_float2(-p.cap_c, -p.cap_c);
+          auto exp_fixed = [&](auto poly_tag, auto mask_tag) {
+            constexpr bool kP = decltype(poly_tag)::value, kM = decltype(mask_tag)::value;
+            const float2 q0 = make_float2(p.cap_q[0], p.cap_q[0]), q1 = make_float2(p.cap_q[1], p.cap_q[1]);
+            const float2 q2 = make_float2(p.cap_q[2], p.cap_q[2]), q3 = make_float2(p.cap_q[3], p.cap_q[3]);
 #pragma unroll
-        for (int u = 0; u < kMx; ++u) mxs[u] = -INFINITY;
-        if (poly) {
-          // the maximum is known
-        } else if (masked) {
-          uint32_t w[4];
-          if (ivl_ok && cls != FFA_TILE_FULL) {
-            const int c0 = kt * kTile;
-            w[0] = w[1] = w[2] = w[3] = 0u;
-            if (cls == FFA_TILE_PARTIAL) {
-              set_bits(w, max(ilo0 - c0, 0), min(ihi0 - c0, kTile));
-              set_bits(w, max(ilo1 - c0, 0), min(ihi1 - c0, kTile));
+            for (int c4 = 0; c4 < 4; ++c4) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const float2 s2 = make_float2(__uint_as_float(sv[c4][2 * k]), __uint_as_float(sv[c4][2 * k + 1]));
+                float2 y;
+                if constexpr (kP) {
+                  const float2 t = mul2(s2, s2);
+                  y = fma2(s2, fma2(fma2(fma2(q3, t, q2), t, q1), t, q0), nm2);
+                } else {
+                  y = add2(s2, nm2);
+                }
+                if constexpr (kM) {
+                  y.x = ((w[c4] >> (2 * k)) & 1u) ? y.x : -INFINITY;
+                  y.y = ((w[c4] >> (2 * k + 1)) & 1u) ? y.y : -INFINITY;
+                }
+                const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+                sum2[k & 1] = add2(sum2[k & 1], make_float2(p0, p1));
+                pk[k] = pack_bf16x2(p0, p1);
+                if constexpr (kM)
+                  sumr2[k & 1] = add2(sumr2[k & 1], make_float2(__uint_as_float(pk[k] << 16),
+                                                                __uint_as_float(pk[k] & 0xffff0000u)));
+              }
+              tmem_st16(tS + 16 * c4, pk);
             }
-            const int valid = p.nk - c0;
-            if (valid < kTile) {
-              uint32_t t4[4] = {0u, 0u, 0u, 0u};
-              set_bits(t4, 0, valid);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) w[k] &= t4[k];
+          };
+          if (poly_f) {
+            if (masked) {
+              exp_fixed(std::true_type{}, std::true_type{});
+            } else {
+              exp_fixed(std::true_type{}, std::false_type{});
             }
           } else {
-            row_mask(p, cls, row, kt, nsl, sl, w);
+            if (masked) {
+              exp_fixed(std::false_type{}, std::true_type{});
+            } else {
+              exp_fixed(std::false_type{}, std::false_type{});
+            }
           }
-#pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            float x = __uint_as_float(sv[c >> 5][c & 31]);
-            if (kCap) x = capped_log2(x, p.cap_c, p.cap_k);
-            if (kBias) x = (kCap ? x : x * p.scale_log2) + fmaf(slope_log2, static_cast<float>(c), bbase);
-            x = ((w[c >> 5] >> (c & 31)) & 1u) ? x : -INFINITY;
-            sv[c >> 5][c & 31] = __float_as_uint(x);
-            mxs[c % kMx] = fmaxf(mxs[c % kMx], x);
+          const float tile_l = (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
+          l_run += tile_l;
+          if (masked) {
+            r_run += (sumr2[0].x + sumr2[0].y) + (sumr2[1].x + sumr2[1].y);
+          } else {
+            // the sum of the bf16 values the PV MMA uses, as the fp32 sum plus the rounding
+            // error of the tile's largest p (the only one that can dominate a row), recomputed
+            // with the exponential pass's exact operations
+            const float t = smax * smax;
+            const float y_max = poly_f ? fmaf(smax, fmaf(fmaf(fmaf(p.cap_q[3], t, p.cap_q[2]), t, p.cap_q[1]), t, p.cap_q[0]), -p.cap_c)
+                                       : capped_log2(smax, p.cap_c, p.cap_k) + (-p.cap_c);
+            const float p_max = ex2_approx(y_max);
+            r_run += tile_l + (__uint_as_float(pack_bf16x2(p_max, 0.0f) << 16) - p_max);
           }
         } else {
+          // ALiBi in the log2 domain: slope * log2(e) * (key - row) = bbase + slope * log2(e) * c
+          const float bbase = kBias ? slope_log2 * static_cast<float>(kt * kTile - a_pos) : 0.0f;
+          // Softcap on a fully visible tile: when every raw score of the warp's rows lies where
+          // the tanh polynomial holds, the logits are formed inside the exponential pass (FMA
+          // pipe only), and the row max is the polynomial at the raw max, the transform being
+          // increasing there.  Otherwise (and on masked tiles) the exact transform runs first.
+          constexpr bool kPolyCap = kCap && !kBias;
+          bool poly = false;
+          float mx = -INFINITY, smax_p = -INFINITY;
+          if (kPolyCap && !masked) {
+            float hi[4], lo[4];
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            float x = __uint_as_float(sv[c >> 5][c & 31]);
-            if (kCap) x = capped_log2(x, p.cap_c, p.cap_k);
-            if (kBias) x = (kCap ? x : x * p.scale_log2) + fmaf(slope_log2, static_cast<float>(c), bbase);
-            if (kPre) sv[c >> 5][c & 31] = __float_as_uint(x);
-            mxs[c % kMx] = fmaxf(mxs[c % kMx], x);
-          }
-        }
-        if (!poly) {
-          mx = mxs[0];
-#pragma unroll
-          for (int u = 1; u < kMx; ++u) mx = fmaxf(mx, mxs[u]);
-        }
-        const float m_tile = kPre ? mx : mx * p.scale_log2;
-        const bool need = m_tile > m_run + kTau;
-        const bool rescale = need && (m_run != -INFINITY);
-        const float alpha = rescale ? ex2_approx(m_run - m_tile) : 1.0f;
-        if (need) m_run = m_tile;
-        if (rescale) {
-          l_run *= alpha;
-          r_run *= alpha;
-        }
-        const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
-        // exponentials two columns at a time: the argument and both running sums use packed
-        // fp32 pair instructions; two accumulator pairs each shorten the addition chains
-        float2 sum2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-        float2 sumr2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-        const float sc = kPre ? 1.0f : p.scale_log2;
-        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(neg_m, neg_m);
-        auto exp_pass = [&](auto poly_tag) {
-          constexpr bool kP = decltype(poly_tag)::value;
-          float2 q[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) q[i] = kP ? make_float2(p.cap_q[i], p.cap_q[i]) : make_float2(0.0f, 0.0f);
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float2 s2 = make_float2(__uint_as_float(sv[c4][2 * k]), __uint_as_float(sv[c4][2 * k + 1]));
-              float2 y;
-              if constexpr (kP) {
-                const float2 t = mul2(s2, s2);
-                const float2 w = fma2(fma2(fma2(q[3], t, q[2]), t, q[1]), t, q[0]);
-                y = fma2(s2, w, nm2);
-              } else {
-                y = fma2(s2, sc2, nm2);
-              }
-              const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
-              sum2[k & 1] = add2(sum2[k & 1], make_float2(p0, p1));
-              pk[k] = pack_bf16x2(p0, p1);
-              sumr2[k & 1] = add2(sumr2[k & 1], make_float2(__uint_as_float(pk[k] << 16),
-                                                            __uint_as_float(pk[k] & 0xffff0000u)));
+            for (int u = 0; u < 4; ++u) {
+              hi[u] = -INFINITY;
+              lo[u] = INFINITY;
             }
-            tmem_st16(tS + 16 * c4, pk);
+#pragma unroll
+            for (int c = 0; c < 128; c += 2) {
+              const float a = __uint_as_float(sv[c >> 5][c & 31]), b = __uint_as_float(sv[c >> 5][(c & 31) + 1]);
+              hi[(c >> 1) & 3] = fmax3(hi[(c >> 1) & 3], a, b);
+              lo[(c >> 1) & 3] = fmin3(lo[(c >> 1) & 3], a, b);
+            }
+            const float smax = fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3]));
+            const float smin = fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3]));
+            poly = __all_sync(0xffffffffu, fmaxf(smax, -smin) <= p.cap_slim);
+            if (poly) {
+              const float t = smax * smax;
+              mx = smax * fmaf(fmaf(fmaf(p.cap_q[3], t, p.cap_q[2]), t, p.cap_q[1]), t, p.cap_q[0]);
+              smax_p = smax;
+            }
           }
-        };
-        if constexpr (kPolyCap) {
+          // row max: eight independent partial maxima when the logits are formed first (a
+          // longer transform per element), one chain otherwise (measured faster there)
+          constexpr int kMx = kPre ? 8 : 1;
+          float mxs[kMx];
+#pragma unroll
+          for (int u = 0; u < kMx; ++u) mxs[u] = -INFINITY;
           if (poly) {
-            exp_pass(std::true_type{});
+            // the maximum is known
+          } else if (masked) {
+            uint32_t w[4];
+            tile_mask(p, cls, row, kt, nsl, sl, ivl_ok, ilo0, ihi0, ilo1, ihi1, w);
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              float x = __uint_as_float(sv[c >> 5][c & 31]);
+              if (kCap) x = capped_log2(x, p.cap_c, p.cap_k);
+              if (kBias) x = (kCap ? x : x * p.scale_log2) + fmaf(slope_log2, static_cast<float>(c), bbase);
+              x = ((w[c >> 5] >> (c & 31)) & 1u) ? x : -INFINITY;
+              sv[c >> 5][c & 31] = __float_as_uint(x);
+              mxs[c % kMx] = fmaxf(mxs[c % kMx], x);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              float x = __uint_as_float(sv[c >> 5][c & 31]);
+              if (kCap) x = capped_log2(x, p.cap_c, p.cap_k);
+              if (kBias) x = (kCap ? x : x * p.scale_log2) + fmaf(slope_log2, static_cast<float>(c), bbase);
+              if (kPre) sv[c >> 5][c & 31] = __float_as_uint(x);
+              mxs[c % kMx] = fmaxf(mxs[c % kMx], x);
+            }
+          }
+          if (!poly) {
+            mx = mxs[0];
+#pragma unroll
+            for (int u = 1; u < kMx; ++u) mx = fmaxf(mx, mxs[u]);
+          }
+          const float m_tile = kPre ? mx : mx * p.scale_log2;
+          const bool need = m_tile > m_run + kTau;
+          rescale = need && (m_run != -INFINITY);
+          alpha = rescale ? ex2_approx(m_run - m_tile) : 1.0f;
+          if (need) m_run = m_tile;
+          if (rescale) {
+            l_run *= alpha;
+            r_run *= alpha;
+          }
+          const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
+          // exponentials two columns at a time: the argument and both running sums use packed
+          // fp32 pair instructions; two accumulator pairs each shorten the addition chains
+          float2 sum2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+          float2 sumr2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+          const float sc = kPre ? 1.0f : p.scale_log2;
+          const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(neg_m, neg_m);
+          auto exp_pass = [&](auto poly_tag) {
+            constexpr bool kP = decltype(poly_tag)::value;
+            float2 q[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q[i] = kP ? make_float2(p.cap_q[i], p.cap_q[i]) : make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const float2 s2 = make_float2(__uint_as_float(sv[c4][2 * k]), __uint_as_float(sv[c4][2 * k + 1]));
+                float2 y;
+                if constexpr (kP) {
+                  const float2 t = mul2(s2, s2);
+                  const float2 w = fma2(fma2(fma2(q[3], t, q[2]), t, q[1]), t, q[0]);
+                  y = fma2(s2, w, nm2);
+                } else {
+                  y = fma2(s2, sc2, nm2);
+                }
+                const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+                sum2[k & 1] = add2(sum2[k & 1], make_float2(p0, p1));
+                pk[k] = pack_bf16x2(p0, p1);
+                if constexpr (kBias)
+                  sumr2[k & 1] = add2(sumr2[k & 1], make_float2(__uint_as_float(pk[k] << 16),
+                                                                __uint_as_float(pk[k] & 0xffff0000u)));
+              }
+              tmem_st16(tS + 16 * c4, pk);
+            }
+          };
+          if constexpr (kPolyCap) {
+            if (poly) {
+              exp_pass(std::true_type{});
+            } else {
+              exp_pass(std::false_type{});
+            }
           } else {
             exp_pass(std::false_type{});
           }
-        } else {
-          exp_pass(std::false_type{});
+          const float tile_l = (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
+          l_run += tile_l;
+          if constexpr (kBias) {
+            r_run += (sumr2[0].x + sumr2[0].y) + (sumr2[1].x + sumr2[1].y);
+          } else {
+            // the fp32 sum plus the rounding error of the tile's largest p, recomputed with the
+            // exponential pass's exact operations (its argument is the largest one)
+            float y_max;
+            if (poly) {
+              const float t = smax_p * smax_p;
+              y_max = fmaf(smax_p, fmaf(fmaf(fmaf(p.cap_q[3], t, p.cap_q[2]), t, p.cap_q[1]), t, p.cap_q[0]), neg_m);
+            } else {
+              y_max = fmaf(mx, sc, neg_m);
+            }
+            const float p_max = ex2_approx(y_max);
+            r_run += tile_l + (__uint_as_float(pack_bf16x2(p_max, 0.0f) << 16) - p_max);
+          }
         }
-        l_run += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
-        r_run += (sumr2[0].x + sumr2[0].y) + (sumr2[1].x + sumr2[1].y);
         // Rescale this row of O when its reference max moved.  O is stable here: the S MMA
         // that produced this tile was issued after the previous PV MMA, and the next PV MMA
         // waits for this warpgroup's p_full arrival below.
@@ -800,10 +927,10 @@ __global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
 }
 
 
-template <int D, bool kCap, bool kBias>
+template <int D, bool kCap, bool kBias, bool kFixed>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   using SM = FwdSmem<D>;
-  auto kern = ffa_fwd_kernel<D, kCap, kBias>;
+  auto kern = ffa_fwd_kernel<D, kCap, kBias, kFixed>;
   // Once per device (the shared-memory attribute applies to the device current when it is
   // set).  The register split (setmaxnreg) is balanced for exactly kRegsLaunch registers per
   // thread at launch; with any other count a softmax warp's increase could never be granted,
@@ -838,6 +965,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.cap_c = a.softcap * kLog2e;
   p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
   fold_cap_poly(a.scale, a.softcap, p.cap_q, &p.cap_slim);
+  p.cap_fixed = (a.softcap > 0.0f && 2.0f * p.cap_c <= 120.0f) ? 1 : 0;
   p.plan = a.plan;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
@@ -865,12 +993,16 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
   const bool cap = a.softcap > 0.0f, bias = a.alibi != nullptr;
+  // a bounded softcap without ALiBi takes the fixed-reference kernel (FwdParams::cap_fixed)
+  const bool fixed = cap && !bias && 2.0f * a.softcap * kLog2e <= 120.0f;
   if (a.P.d == 64) {
-    if (bias) return cap ? launch_impl<64, true, true>(a, s) : launch_impl<64, false, true>(a, s);
-    return cap ? launch_impl<64, true, false>(a, s) : launch_impl<64, false, false>(a, s);
+    if (bias) return cap ? launch_impl<64, true, true, false>(a, s) : launch_impl<64, false, true, false>(a, s);
+    if (fixed) return launch_impl<64, true, false, true>(a, s);
+    return cap ? launch_impl<64, true, false, false>(a, s) : launch_impl<64, false, false, false>(a, s);
   }
-  if (bias) return cap ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
-  return cap ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
+  if (bias) return cap ? launch_impl<128, true, true, false>(a, s) : launch_impl<128, false, true, false>(a, s);
+  if (fixed) return launch_impl<128, true, false, true>(a, s);
+  return cap ? launch_impl<128, true, false, false>(a, s) : launch_impl<128, false, false, false>(a, s);
 }
 
 }  // namespace ffa
