@@ -423,6 +423,32 @@ def time_calls(w: W.Workload, calls: int, phase: str):
             **{f"{ph}_ms_median": round(statistics.median(x), 4) for ph, x in t.items() if x}}
 
 
+def time_decode(ffa, dw, dev, flush, iters: int, warm: int):
+    """Whole ffa_fwd_decode calls on a decoding batch (packing, slices, attention, merge,
+    unpacking), L2 flushed before each; milliseconds of the timed calls."""
+    q_h, k_h, v_h = dw.draw()
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    qr, kr, ty = (torch.tensor(x, dtype=torch.int32, device=dev) for x in dw.slices())
+    out = torch.empty_like(q)
+    lse = torch.empty(dw.hq, dw.total_q, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = None
+    t = []
+    for i in range(warm + iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        e0.record()
+        out, lse = ffa.ffa_fwd_decode(q, k, v, qr, kr, ty, max_seqlen_q=dw.q_len, out=out, lse=lse, workspace=ws,
+                                      status=st)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= warm:
+            t.append(e0.elapsed_time(e1))
+    if int(st.item()) != 0:
+        raise RuntimeError(f"{dw.name}: device status {int(st.item())}")
+    return t
+
+
 def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
     """Every workload of the project timed alone on this GPU: the whole forward call (planner,
     kernel, merge) and backward call (planner, preprocess, kernel, dq conversion) with CUDA
@@ -493,6 +519,15 @@ def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
         res[name] = e
         del q, k, v, do, out, lse, dq, dk, dv, wsf, wsb
         torch.cuda.empty_cache()
+    for name, dw in W.DECODE.items():
+        ms = statistics.median(time_decode(ffa, dw, dev, flush, iters, warm))
+        kv_bytes = 2 * dw.total_k * dw.hkv * dw.d * 2
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        res[name] = {"sequences": dw.n_seq, "new_tokens": dw.q_len, "keys_per_sequence": dw.kv_len,
+                     "heads": f"{dw.hq}/{dw.hkv}", "d": dw.d, "ms": round(ms, 4), "us": round(ms * 1e3, 1),
+                     "kv_bytes": kv_bytes, "hbm_gbs": round(gbs, 1),
+                     "frac_hbm": round(gbs / float(peaks.get("hbm_gbs", 6800.0)), 4)}
+        torch.cuda.empty_cache()
     res["_timing"] = (f"median of {iters} calls after {warm} warm-up calls; L2 flushed (256 MiB write) before "
                       "every timed call; 'ms' = whole call (planner included), 'kernel_ms' = main kernel alone; "
                       f"peaks: burst {peak_b}, sustained {peak_s} TFLOP/s")
@@ -505,10 +540,10 @@ def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
 # source changes the figure no longer describes the kernel, and `traffic` is reported null.
 TRAFFIC = {
     # (workload, kernel): (bytes per launch, source hash at capture)
-    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1810359552 + 234913792, "10bfa9534f737a60"),
-    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (12508939008 + 5972337408, "f3a33f7eda8f2c7b"),
-    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541674240 + 236363008, "10bfa9534f737a60"),
-    ("sliding_32k_softcap", "ffa_bwd_kernel"): (6672052480 + 3488093184, "f3a33f7eda8f2c7b"),
+    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1794624256 + 236418560, "fba897a95d12b208"),
+    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (12657694208 + 5986946560, "f3a33f7eda8f2c7b"),
+    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541666304 + 235767808, "fba897a95d12b208"),
+    ("sliding_32k_softcap", "ffa_bwd_kernel"): (6585803264 + 3452497664, "f3a33f7eda8f2c7b"),
 }
 
 
@@ -650,7 +685,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="long_causal_64k_prefix", choices=sorted(W.ALL))
+    ap.add_argument("--workload", default="long_causal_64k_prefix", choices=sorted(W.ALL) + sorted(W.DECODE))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload table")
     ap.add_argument("--oracle-report", action="store_true",
@@ -669,6 +704,13 @@ def main():
         return
     if args.warmup < 3:
         args.warmup = 3
+    if args.calls > 0 and args.workload in W.DECODE:
+        import flexible_mask_attention_range_gb300 as ffa
+        dev = torch.device("cuda", 0)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        t = time_decode(ffa, W.DECODE[args.workload], dev, flush, args.calls, 0)
+        print(json.dumps({"workload": args.workload, "calls": args.calls, "ms_median": statistics.median(t)}))
+        return
     w = W.get(args.workload)
     if args.calls > 0:
         print(json.dumps(time_calls(w, args.calls, args.phase)), flush=True)

@@ -678,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (in_rows) p.lse[static_cast<size_t>(h) * p.nq + row] = lse_row;
       } else {
         // one chunk of a split row: normalised partial O (fp32) and its LSE for the merge
+        // (rows past the end are never merged)
         const size_t prow = (static_cast<size_t>(it.pslot) * p.slots + it.slot) * 2 * kTile + wg * kTile + r;
         float4* dst = reinterpret_cast<float4*>(p.plan.part_o + prow * D);
 #pragma unroll
@@ -686,12 +687,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tO + 32 * c, o);
           tmem_wait_ld();
           reg_fence(o);
+          if (in_rows) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[8 * c + k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
-                                         __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+            for (int k = 0; k < 8; ++k)
+              dst[8 * c + k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                                           __uint_as_float(o[4 * k + 2]) * inv_l,
+                                           __uint_as_float(o[4 * k + 3]) * inv_l);
+          }
         }
-        p.plan.part_lse[prow] = lse_row;
+        if (in_rows) p.plan.part_lse[prow] = lse_row;
       }
     }
     if (!ok) record_abort(abort_flag, p.status);
@@ -871,24 +875,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 // LSE merge of split rows: for a group whose work list was cut into chunks, every row combines
 // its chunks' partial results, L = log sum_c e^{L_c} and O = sum_c e^{L_c - L} O_c (the
 // chunks cover disjoint key sets of the row); rows whose chunks all have L_c = -inf get
-// O = 0 and L = -inf.  One CTA per (group, head slot, sub-tile, 32-row block, 32-column
-// block); thread = (row, 4 columns), so a warp reads whole 128-byte lines of 4 rows.
-constexpr int kMergeRows = 32;
+// O = 0 and L = -inf.  One block per (group, head slot, sub-tile, row): its eight warps take
+// every eighth chunk, a lane holds D / 32 columns (coalesced loads of a partial row), and the
+// warps' sums are combined in shared memory.  Rows past the end return at once.
+constexpr int kMergeWarps = 8;
 template <int D>
-__global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
-  constexpr int kColBlocks = D / 32;
+__global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParams p) {
+  constexpr int kPer = D / 32;  // columns per lane
+  __shared__ float sh_acc[kMergeWarps][D];
+  __shared__ float sh_w[kMergeWarps];
+  __shared__ float sh_max[kMergeWarps];
   int b = blockIdx.x;
-  const int cb = b % kColBlocks;
-  b /= kColBlocks;
-  const int rb = b % (kTile / kMergeRows);
-  b /= kTile / kMergeRows;
+  const int r = b % kTile;
+  b /= kTile;
   const int sub = b & 1;
   b >>= 1;
   const int g = b / p.slots, slot = b - (b / p.slots) * p.slots;
   const int nch = p.plan.grp_nch[g];
   if (nch <= 1) return;
-  const int ps = p.plan.grp_pslot[g];
-  const int r = rb * kMergeRows + (threadIdx.x >> 3), c4 = (threadIdx.x & 7) * 4 + cb * 32;
   int qt, h;
   if (p.head_pair) {
     qt = g;
@@ -899,33 +903,72 @@ __global__ void __launch_bounds__(256) ffa_fwd_merge(const FwdParams p) {
   }
   const int row = qt * kTile + r;
   if (row >= p.nq) return;
+  const int ps = p.plan.grp_pslot[g];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto prow = [&](int c) { return (static_cast<size_t>(ps + c) * p.slots + slot) * 2 * kTile + sub * kTile + r; };
+  // the largest chunk LSE
   float mx = -INFINITY;
-  for (int c = 0; c < nch; ++c) mx = fmaxf(mx, p.plan.part_lse[prow(c)]);
-  uint2* dst = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D + c4);
-  const bool lse_writer = (cb == 0) && ((threadIdx.x & 7) == 0);
+  for (int c = threadIdx.x; c < nch; c += blockDim.x) mx = fmaxf(mx, p.plan.part_lse[prow(c)]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) sh_max[warp] = mx;
+  __syncthreads();
+  mx = sh_max[0];
+#pragma unroll
+  for (int w = 1; w < kMergeWarps; ++w) mx = fmaxf(mx, sh_max[w]);
+  __nv_bfloat16* out = p.out + (static_cast<size_t>(row) * p.hq + h) * D;
   if (mx == -INFINITY) {
-    *dst = make_uint2(0u, 0u);
-    if (lse_writer) p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
+    if (warp == 0) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) out[lane * kPer + k] = __float2bfloat16(0.0f);
+      if (lane == 0) p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
+    }
     return;
   }
-  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.0f;
   float wsum = 0.0f;
-  for (int c = 0; c < nch; ++c) {
+#pragma unroll 4
+  for (int c = warp; c < nch; c += kMergeWarps) {
     const size_t pr = prow(c);
     const float w = ex2_approx((p.plan.part_lse[pr] - mx) * kLog2e);
     wsum += w;
-    const float4 v = *reinterpret_cast<const float4*>(p.plan.part_o + pr * D + c4);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+    const float* src = p.plan.part_o + pr * D + lane * kPer;
+    if constexpr (kPer == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+      acc[2] = fmaf(w, v.z, acc[2]);
+      acc[3] = fmaf(w, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+    }
   }
-  const float inv = 1.0f / wsum;
-  *dst = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  if (lse_writer) p.lse[static_cast<size_t>(h) * p.nq + row] = mx + lg2_approx(wsum) * kLn2;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) sh_acc[warp][lane * kPer + k] = acc[k];
+  if (lane == 0) sh_w[warp] = wsum;
+  __syncthreads();
+  if (warp == 0) {
+    float tw = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) tw += sh_w[w];
+    const float inv = 1.0f / tw;
+#pragma unroll
+    for (int k = 0; k < kPer; k += 2) {
+      float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kMergeWarps; ++w) {
+        a0 += sh_acc[w][lane * kPer + k];
+        a1 += sh_acc[w][lane * kPer + k + 1];
+      }
+      *reinterpret_cast<uint32_t*>(out + lane * kPer + k) = pack_bf16x2(a0 * inv, a1 * inv);
+    }
+    if (lane == 0) p.lse[static_cast<size_t>(h) * p.nq + row] = mx + lg2_approx(tw) * kLn2;
+  }
 }
-
 
 template <int D, bool kCap, bool kBias, bool kFixed>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
@@ -985,7 +1028,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   if (g_kernel_events.fwd_stop != nullptr) cudaEventRecord(g_kernel_events.fwd_stop, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !a.split) return e;
-  ffa_fwd_merge<D><<<a.ngrp * a.slots * 2 * (kTile / kMergeRows) * (D / 32), 256, 0, stream>>>(p);
+  ffa_fwd_merge<D><<<a.ngrp * a.slots * 2 * kTile, 32 * kMergeWarps, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

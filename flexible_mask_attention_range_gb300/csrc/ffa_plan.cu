@@ -164,11 +164,11 @@ __device__ SliceList gather_slices(const PlanView& v, int n_valid, bool by_col, 
         sm_s[pos] = s;
         sm_t[pos] = t;
       }
-      if (pos < kSliceCap) g_sl[pos] = r;
+      if (pos < kSliceCap && g_sl != nullptr) g_sl[pos] = r;
     }
     count += total;
   }
-  if (threadIdx.x == 0) *g_nsl = count <= kSliceCap ? count : -1;
+  if (threadIdx.x == 0 && g_nsl != nullptr) *g_nsl = count <= kSliceCap ? count : -1;
   __syncthreads();
   SliceList L;
   if (count <= kSliceSmem) {
@@ -184,42 +184,44 @@ __device__ SliceList gather_slices(const PlanView& v, int n_valid, bool by_col, 
 }
 
 // ---------------------------------------------------------------- 2. forward rows
-// One block per forward group.  head_pair: the group is one query tile; otherwise it is the
-// query-tile pair (2g, 2g+1) whose work list is the union of both rows.
-__global__ void __launch_bounds__(256) plan_rows_kernel(ProblemDims P, int head_pair, PlanView v) {
+// Classification: one block per (query tile, range of kPlanSpan key tiles), so that rows with
+// many key tiles (decoding batches: one query tile, thousands of key tiles) are classified
+// by many blocks.  The block with the first range also stores the tile row's slice list.
+constexpr int kPlanSpan = 256;
+__global__ void __launch_bounds__(256) plan_row_classes_kernel(ProblemDims P, PlanView v) {
   __shared__ int4 sm_s[kSliceSmem];
   __shared__ int sm_t[kSliceSmem];
-  __shared__ uint8_t sm_cls[2][kMaxTiles];
+  __shared__ int warp_buf[32];
+  const int qt = blockIdx.x;
+  const int k0 = blockIdx.y * kPlanSpan, k1 = min(P.nkt, k0 + kPlanSpan);
+  const int n_valid = v.hdr[0];
+  const int r0 = qt * kTile, r1 = min(r0 + kTile, P.nq);
+  const bool first = blockIdx.y == 0;
+  SliceList L = gather_slices(v, n_valid, false, r0, r1, sm_s, sm_t, warp_buf, first ? &v.row_nsl[qt] : nullptr,
+                              first ? &v.row_sl[static_cast<size_t>(qt) * kSliceCap] : nullptr);
+  for (int kt = k0 + threadIdx.x; kt < k1; kt += blockDim.x) {
+    const int c0 = kt * kTile, c1 = min(c0 + kTile, P.nk);
+    const int c = L.n ? classify_tile(L, r0, r1, c0, c1) : FFA_TILE_EMPTY;
+    v.cls[static_cast<size_t>(qt) * P.nkt + kt] = static_cast<uint8_t>(c);
+  }
+}
+
+// Work lists: one block per forward group.  head_pair: the group is one query tile; otherwise
+// it is the query-tile pair (2g, 2g+1) whose work list is the union of both rows.  Entries:
+// key tiles non-empty for either sub-tile, ascending, with both sub-tiles' classes.
+__global__ void __launch_bounds__(256) plan_row_lists_kernel(ProblemDims P, int head_pair, PlanView v) {
   __shared__ int warp_buf[32];
   const int g = blockIdx.x;
-  const int n_valid = v.hdr[0];
-  const int nsub = head_pair ? 1 : 2;
-  for (int sub = 0; sub < nsub; ++sub) {
-    const int qt = head_pair ? g : 2 * g + sub;
-    if (qt >= P.nqt) {
-      for (int kt = threadIdx.x; kt < P.nkt; kt += blockDim.x) sm_cls[sub][kt] = FFA_TILE_EMPTY;
-      __syncthreads();
-      continue;
-    }
-    const int r0 = qt * kTile, r1 = min(r0 + kTile, P.nq);
-    SliceList L = gather_slices(v, n_valid, false, r0, r1, sm_s, sm_t, warp_buf, &v.row_nsl[qt],
-                                &v.row_sl[static_cast<size_t>(qt) * kSliceCap]);
-    for (int kt = threadIdx.x; kt < P.nkt; kt += blockDim.x) {
-      const int c0 = kt * kTile, c1 = min(c0 + kTile, P.nk);
-      const int c = L.n ? classify_tile(L, r0, r1, c0, c1) : FFA_TILE_EMPTY;
-      sm_cls[sub][kt] = static_cast<uint8_t>(c);
-      v.cls[static_cast<size_t>(qt) * P.nkt + kt] = static_cast<uint8_t>(c);
-    }
-    __syncthreads();
-  }
-  // work list: key tiles non-empty for either sub-tile, ascending
+  const int qa = head_pair ? g : 2 * g, qb = head_pair ? g : 2 * g + 1;
+  const uint8_t* ca_row = v.cls + static_cast<size_t>(qa) * P.nkt;
+  const uint8_t* cb_row = qb < P.nqt ? v.cls + static_cast<size_t>(qb) * P.nkt : nullptr;
   int count = 0;
   for (int c = 0; c < P.nkt; c += blockDim.x) {
     const int kt = c + threadIdx.x;
     int ca = 0, cb = 0;
     if (kt < P.nkt) {
-      ca = sm_cls[0][kt];
-      cb = head_pair ? ca : sm_cls[1][kt];
+      ca = ca_row[kt];
+      cb = head_pair ? ca : (cb_row != nullptr ? cb_row[kt] : FFA_TILE_EMPTY);
     }
     const int keep = (ca | cb) != 0;
     int total;
@@ -387,8 +389,11 @@ cudaError_t launch_plan_slices(const ProblemDims& P, const int32_t* q_ranges, co
 
 cudaError_t launch_plan_rows(const ProblemDims& P, const WsLayout& L, const PlanView& v, cudaStream_t s) {
   if (L.ngrp == 0) return cudaSuccess;
-  plan_rows_kernel<<<L.ngrp, 256, 0, s>>>(P, L.head_pair ? 1 : 0, v);
+  plan_row_classes_kernel<<<dim3(P.nqt, (P.nkt + kPlanSpan - 1) / kPlanSpan), 256, 0, s>>>(P, v);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  plan_row_lists_kernel<<<L.ngrp, 256, 0, s>>>(P, L.head_pair ? 1 : 0, v);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem = static_cast<size_t>(L.split_len + 1) * sizeof(int);
   plan_chunks_kernel<<<1, 1024, smem, s>>>(L.ngrp, L.split_len, v);

@@ -211,3 +211,47 @@ def random_page_table(n_logical: int, n_pages: int, seed: int) -> torch.Tensor:
     random permutation prefix), int32 -- the page table of a paged key/value cache."""
     g = make_generator(seed)
     return torch.randperm(n_pages, generator=g)[:n_logical].to(torch.int32)
+
+# --------------------------------------------------------------------------------------
+# Decoding batches: n_seq sequences, each with q_len new query tokens at the end of its
+# kv_len keys (one CAUSAL slice per sequence: bottom-right alignment makes the new tokens see
+# every earlier key), packed one sequence after another on both token axes.
+# --------------------------------------------------------------------------------------
+
+@dataclass
+class DecodeWorkload:
+    name: str
+    n_seq: int
+    q_len: int
+    kv_len: int
+    hq: int
+    hkv: int
+    d: int
+    seed: int
+
+    @property
+    def total_q(self) -> int:
+        return self.n_seq * self.q_len
+
+    @property
+    def total_k(self) -> int:
+        return self.n_seq * self.kv_len
+
+    def slices(self):
+        qr = [(s * self.q_len, (s + 1) * self.q_len) for s in range(self.n_seq)]
+        kr = [(s * self.kv_len, (s + 1) * self.kv_len) for s in range(self.n_seq)]
+        return qr, kr, [CAUSAL] * self.n_seq
+
+    def draw(self):
+        """q [n_seq * q_len, Hq, d], k, v [n_seq * kv_len, Hkv, d]: bf16 N(0,1), seeded."""
+        g = make_generator(self.seed)
+        q = torch.randn(self.total_q, self.hq, self.d, generator=g).to(torch.bfloat16)
+        k = torch.randn(self.total_k, self.hkv, self.d, generator=g).to(torch.bfloat16)
+        v = torch.randn(self.total_k, self.hkv, self.d, generator=g).to(torch.bfloat16)
+        return q, k, v
+
+
+DECODE = {w.name: w for w in (
+    DecodeWorkload("decode_64x8k_g4", n_seq=64, q_len=1, kv_len=8192, hq=16, hkv=4, d=128, seed=11),
+    DecodeWorkload("decode_8x64k_g8", n_seq=8, q_len=1, kv_len=65536, hq=16, hkv=2, d=128, seed=12),
+)}
