@@ -397,6 +397,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence(sv[c]);
         const bool masked = (cls != FFA_TILE_FULL) || (kt * kTile + kTile > p.nk);
+        // element mask of this row over the tile (bit c: key kt * 128 + c visible)
+        uint32_t wm[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (!kFixed && masked) {  // (the bounded-softcap kernel masks inside its own pass)
+          tile_mask(p, cls, row, kt, nsl, sl, ivl_ok, ilo0, ihi0, ilo1, ihi1, wm);
+          // none of the warp's 32 rows sees a key of this tile (a decoding batch's tile
+          // belongs to one sequence; rows past the end): P = 0, nothing else changes
+          if (__all_sync(0xffffffffu, (wm[0] | wm[1] | wm[2] | wm[3]) == 0u)) {
+            const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) tmem_st16(tS + 16 * c4, z);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[wg]);
+            continue;
+          }
+        }
         bool rescale = false;  // the reference max moved: O rows are scaled by alpha
         float alpha = 1.0f;
         if constexpr (kFixed) {
@@ -530,8 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (poly) {
             // the maximum is known
           } else if (masked) {
-            uint32_t w[4];
-            tile_mask(p, cls, row, kt, nsl, sl, ivl_ok, ilo0, ihi0, ilo1, ihi1, w);
+            const uint32_t(&w)[4] = wm;
 #pragma unroll
             for (int c = 0; c < 128; ++c) {
               float x = __uint_as_float(sv[c >> 5][c & 31]);
