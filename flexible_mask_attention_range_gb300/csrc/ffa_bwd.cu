@@ -212,8 +212,14 @@ __device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t sDS, uint32_t
 }
 
 struct BwdItem {
-  int kt, kvh, n_ent, n_steps;
+  int kt, kvh, n_ent, n_steps, rot;
   const uint32_t* ents;
+  // the item's e-th entry in processing order: the list rotated so that it starts at the
+  // query tile that is a multiple of its length (see decode_item)
+  __device__ __forceinline__ uint32_t ent(int e) const {
+    const int i = e + rot;
+    return ents[i < n_ent ? i : i - n_ent];
+  }
 };
 
 __device__ __forceinline__ BwdItem decode_item(const BwdParams& p, int item) {
@@ -224,6 +230,16 @@ __device__ __forceinline__ BwdItem decode_item(const BwdParams& p, int item) {
   it.n_ent = p.plan.col_cnt[it.kt];
   it.n_steps = it.n_ent * p.G;
   it.ents = p.plan.col_ent + static_cast<size_t>(it.kt) * p.nqt;
+  // Rotation (not in deterministic mode, whose additions follow ascending key tiles): a list
+  // of n consecutive query tiles starts at the one whose index is a multiple of n, so CTAs on
+  // neighbouring key tiles with lists of the same length (a sliding window, or the tails of
+  // causal columns) work on the same query tile at the same time and share its Q, dO and dq
+  // accumulator in L2.  Any other list is only rotated; every entry is still visited once.
+  it.rot = 0;
+  if (!p.det && it.n_ent > 1) {
+    const int r = entry_idx(it.ents[0]) % it.n_ent;
+    it.rot = r == 0 ? 0 : it.n_ent - r;
+  }
   return it;
 }
 
@@ -326,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nsl = p.plan.col_nsl[it.kt];
       const int* sl = p.plan.col_sl + static_cast<size_t>(it.kt) * kSliceCap;
       for (int t = 0; t < it.n_steps && ok; ++t) {
-        const uint32_t e = it.ents[t / p.G];
+        const uint32_t e = it.ent(t / p.G);
         const int qt = entry_idx(e);
         const int cls = entry_cls(e, 0);
         const uint32_t st = step_cnt % S;
@@ -557,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item >= p.n_items) break;
       const BwdItem it = decode_item(p, item);
       for (int t = 0; t < it.n_steps; ++t) {
-        const int qt = entry_idx(it.ents[t / p.G]);
+        const int qt = entry_idx(it.ent(t / p.G));
         const int h = it.kvh * p.G + (t % p.G);
         // one decision for the whole warpgroup: it meets again at named barrier 1 below
         ok = named_bar_and(1, 128, mbar_wait(dq_full, step_cnt & 1u, abort_flag, lim));
@@ -648,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         last_kv = static_cast<int>(item_cnt);
         for (int t = 0; t < it.n_steps; ++t) {
-          const int qt = entry_idx(it.ents[t / p.G]);
+          const int qt = entry_idx(it.ent(t / p.G));
           const int h = it.kvh * p.G + (t % p.G);
           const uint32_t st = gq % S, u = gq / S;
           if (u > 0) {

@@ -50,22 +50,25 @@ def _inputs():
     return w, q, k, v, do
 
 
-def test_forward_wait_runs_out_then_next_call_is_correct():
+# softcap 30 takes the bounded-softcap kernel instance (fixed reference, no row max), 0 the
+# general one
+@pytest.mark.parametrize("softcap", [0.0, 30.0])
+def test_forward_wait_runs_out_then_next_call_is_correct(softcap):
     w, q, k, v, _ = _inputs()
     qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     with _stalled():
         t0 = time.perf_counter()
-        ffa.ffa_fwd(qc, kc, vc, w.q_ranges, w.k_ranges, w.types, status=st)
+        ffa.ffa_fwd(qc, kc, vc, w.q_ranges, w.k_ranges, w.types, softcap=softcap, status=st)
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
     assert int(st.item()) & ffa.STATUS_TIMEOUT
     assert dt < 10.0
     st.zero_()
-    out, lse = ffa.ffa_fwd(qc, kc, vc, w.q_ranges, w.k_ranges, w.types, status=st)
+    out, lse = ffa.ffa_fwd(qc, kc, vc, w.q_ranges, w.k_ranges, w.types, softcap=softcap, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    ro, rl = O.forward(q, k, v, w.q_ranges, w.k_ranges, w.types)
+    ro, rl = O.forward(q, k, v, w.q_ranges, w.k_ranges, w.types, softcap=softcap)
     assert_out_close(to64(out), ro)
     assert_lse_close(to64(lse), rl)
 
