@@ -66,13 +66,17 @@ struct FwdSmem {
   static constexpr int kQ1 = kTileBytes;
   static constexpr int kK = 2 * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
+  // output staging: one 128-row x 64-column bf16 box per softmax warpgroup
+  static constexpr int kOst = kV + kStages * kTileBytes;
+  static constexpr int kOstBytes = kTile * 128;
+  static constexpr int kBar = kOst + 2 * kOstBytes;
   // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain,
   // stall (never arrived on; the failure-detection test waits on it)
   static constexpr int kNumBars = 2 + 3 * kStages + 8;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;
+  static_assert(kAlloc <= 232448, "forward shared memory exceeds the per-block limit");
 };
 
 struct FwdParams {
@@ -272,7 +276,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint3
 template <int D, bool kCap, bool kBias, bool kFixed>
 __global__ void __launch_bounds__(kThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const FwdParams p) {
   using SM = FwdSmem<D>;
   constexpr int S = SM::kStages;
   constexpr bool kPre = kCap || kBias;  // logits formed in the log2 domain before the row max
@@ -316,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, 512);
@@ -336,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t tS = tbase + lane_base + wg * 128;
     const uint32_t tO = tbase + lane_base + 256 + wg * D;
+    uint8_t* ost = sm + SM::kOst + wg * SM::kOstBytes;  // this warpgroup's output staging box
+    const bool leader = (q4 == 0 && lane == 0);         // issues the warpgroup's output copies
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     for (int wave = 0; ok; ++wave) {
@@ -662,23 +670,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&p_full[wg]);
       }
-      if (!ok) break;
-      // epilogue: O / l -> bf16, LSE
-      ok = __all_sync(0xffffffffu, mbar_wait(&o_full[wg], o_cnt & 1u, abort_flag, lim));
+      // epilogue: O / l -> bf16, LSE.  The warpgroup's four warps agree on going on (a warp
+      // whose wait ran out still reaches the barrier, after raising the abort flag)
+      if (!ok) record_abort(abort_flag, p.status);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[wg], o_cnt & 1u, abort_flag, lim));
+      ok = named_bar_and(1 + wg, 128, ok);
       if (!ok) break;
       ++o_cnt;
       tc_fence_after();
       const float inv_l = r_run > 0.0f ? 1.0f / r_run : 0.0f;
       const float lse_row = l_run > 0.0f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
       if (it.pslot < 0) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
+        // O through shared memory: each 64-column box of the tile is written row by row into
+        // the staging box (128-byte swizzle: 16-byte chunk k of row r at chunk k ^ (r % 8)) and
+        // stored with one TMA copy, which leaves out the rows past the end
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
-          reg_fence(o);
-          if (in_rows) {
+        for (int b = 0; b < D / 64; ++b) {
+          // the previous copy out of the staging box has read it
+          if (leader) bulk_wait_group_read<0>();
+          named_bar_sync(1 + wg, 128);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 64 * b + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence(o);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               uint4 v;
@@ -686,8 +702,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
               v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
               v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-              dst[4 * c + k] = v;
+              const int chunk = (4 * c + k) ^ (r & 7);
+              *reinterpret_cast<uint4*>(ost + r * 128 + chunk * 16) = v;
             }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1 + wg, 128);
+          if (leader) {
+            tma_store_2d(&tmO, ost, h * D + 64 * b, qt * kTile);
+            bulk_commit_group();
           }
         }
         if (in_rows) p.lse[static_cast<size_t>(h) * p.nq + row] = lse_row;
@@ -714,6 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok) record_abort(abort_flag, p.status);
+    if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // output copies done
   } else {
   reg_dealloc<kRegsProducer>();
   if (warp == kWarpTma) {
@@ -1005,7 +1029,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
     setup_err[dev] = e;
   });
   if (setup_err[dev] != cudaSuccess) return setup_err[dev];
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const auto& P = a.P;
   // paged: K/V maps cover the physical pool, one page of rows per box
   const bool paged = a.page_table != nullptr;
@@ -1013,7 +1037,8 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   const uint32_t kv_box = paged ? static_cast<uint32_t>(a.page_size) : static_cast<uint32_t>(kTile);
   if (!encode_tile_map(&mq, a.q, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile) ||
       !encode_tile_map(&mk, a.k, static_cast<uint64_t>(P.hkv) * D, kv_rows, 64, kv_box) ||
-      !encode_tile_map(&mv, a.v, static_cast<uint64_t>(P.hkv) * D, kv_rows, 64, kv_box))
+      !encode_tile_map(&mv, a.v, static_cast<uint64_t>(P.hkv) * D, kv_rows, 64, kv_box) ||
+      !encode_tile_map(&mo, a.out, static_cast<uint64_t>(P.hq) * D, P.nq, 64, kTile))
     return cudaErrorInvalidValue;
   FwdParams p;
   p.nq = P.nq; p.nk = P.nk; p.hq = P.hq; p.hkv = P.hkv; p.G = P.hq / P.hkv;
@@ -1039,7 +1064,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
   if (grid <= 0) return cudaSuccess;
   if (g_kernel_events.fwd_start != nullptr) cudaEventRecord(g_kernel_events.fwd_start, stream);
-  kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, mo, p);
   if (g_kernel_events.fwd_stop != nullptr) cudaEventRecord(g_kernel_events.fwd_stop, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !a.split) return e;
