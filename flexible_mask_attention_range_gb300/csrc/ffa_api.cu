@@ -42,16 +42,6 @@ uint64_t wait_limit_ns() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_shape(const ffa_shape* s, int32_t n_ranges) {
-  if (s == nullptr || n_ranges < 0) return FFA_ERR_INVALID_ARG;
-  if (s->total_q < 0 || s->total_k < 0 || s->num_heads_q < 1 || s->num_heads_kv < 1) return FFA_ERR_INVALID_ARG;
-  if (s->num_heads_q % s->num_heads_kv != 0) return FFA_ERR_INVALID_ARG;
-  if (s->head_dim != 64 && s->head_dim != 128) return FFA_ERR_UNSUPPORTED;
-  if (s->total_q > FFA_MAX_TOKENS || s->total_k > FFA_MAX_TOKENS) return FFA_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(s->num_heads_q) * s->head_dim > 65536) return FFA_ERR_UNSUPPORTED;
-  return FFA_OK;
-}
-
 int check_device() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FFA_ERR_CUDA;
@@ -132,6 +122,16 @@ int num_sms() {
   return cache[dev];
 }
 
+int check_shape(const ffa_shape* s, int32_t n_ranges) {
+  if (s == nullptr || n_ranges < 0) return FFA_ERR_INVALID_ARG;
+  if (s->total_q < 0 || s->total_k < 0 || s->num_heads_q < 1 || s->num_heads_kv < 1) return FFA_ERR_INVALID_ARG;
+  if (s->num_heads_q % s->num_heads_kv != 0) return FFA_ERR_INVALID_ARG;
+  if (s->head_dim != 64 && s->head_dim != 128) return FFA_ERR_UNSUPPORTED;
+  if (s->total_q > FFA_MAX_TOKENS || s->total_k > FFA_MAX_TOKENS) return FFA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(s->num_heads_q) * s->head_dim > 65536) return FFA_ERR_UNSUPPORTED;
+  return FFA_OK;
+}
+
 int check_options(const ffa_options* o) {
   if (o == nullptr) return FFA_OK;
   for (int i = 0; i < 7; ++i)
@@ -162,7 +162,8 @@ int fwd_check(const FwdCall& c, WsLayout* out_layout) {
   if (!aligned16(c.q) || !aligned16(c.k) || !aligned16(c.v) || !aligned16(c.out) ||
       (reinterpret_cast<uintptr_t>(c.lse) & 3u) != 0)
     return FFA_ERR_INVALID_ARG;
-  *out_layout = make_layout(nq, nk, shape->num_heads_q, shape->num_heads_kv, shape->head_dim, c.n_ranges);
+  *out_layout = make_layout(nq, nk, shape->num_heads_q, shape->num_heads_kv, shape->head_dim, c.n_ranges,
+                            c.key_split);
   return FFA_OK;
 }
 
@@ -190,6 +191,7 @@ int fwd_launch(const FwdCall& c, const WsLayout& L, void* scratch) {
   a.slots = L.slots;
   a.n_items = L.ngrp * L.nch_max * L.slots;
   a.split = L.split ? 1 : 0;
+  a.key_split = L.key_split ? 1 : 0;
   a.scale = resolve_scale(c.softmax_scale, d);
   a.softcap = c.softcap;
   a.q = c.q;

@@ -9,11 +9,12 @@
 // query heads, so this library's decoding path packs P query heads of each token into P
 // consecutive rows of a problem with Hq / P heads:
 //     packed row (i * P + g), packed head h  <-  token i, query head h * P + g,
-// with P = G / 2 when G = Hq / Hkv is even (two packed heads per key/value head: they form
-// a head pair of the forward kernel and share every K/V tile it loads) and P = G otherwise.
-// A packed query tile then holds 128 / P tokens, and every key tile is read once per
-// (query tile, key/value head).  Long key sequences with few query tiles are split across
-// CTAs and merged by LSE, as in the plain forward pass.
+// with P = G = Hq / Hkv: one packed head per key/value head.  A packed query tile then holds
+// 128 / G tokens, and every key tile is read once per (query tile, key/value head).  The
+// forward pass runs in its key-split form: a work item is one packed query tile and a chunk of
+// its key tiles, the item's two softmax warpgroups take alternate key tiles, so each key tile
+// meets one 128-row MMA pair instead of two, and each warpgroup leaves a partial result.  The
+// partials of all chunks are merged by LSE, as split rows of the plain forward pass are.
 //
 // Slices are rewritten for the packed rows: a FULL slice [qs, qe) x [ks, ke) becomes
 // [qs * P, qe * P) x [ks, ke); a CAUSAL slice with m = qe - qs query tokens becomes m FULL
@@ -106,8 +107,8 @@ __global__ void __launch_bounds__(256) decode_slices(const int32_t* __restrict__
   }
 }
 
-// Query heads per packed row group: G / 2 for even G (packed heads form head pairs), else G.
-int pack_factor(int G) { return (G % 2 == 0) ? G / 2 : G; }
+// Query heads per packed row group: all G of a key/value head.
+int pack_factor(int G) { return G; }
 
 struct DecodeLayout {
   size_t qp = 0, op = 0, lsep = 0, qr2 = 0, kr2 = 0, ty2 = 0, inner = 0, total = 0;
@@ -130,8 +131,11 @@ bool decode_layout(const ffa_shape* s, int32_t n_ranges, int32_t max_seqlen_q, D
   L->inner_shape.num_heads_q = s->num_heads_q / P;
   L->inner_shape.num_heads_kv = s->num_heads_kv;
   L->inner_shape.head_dim = s->head_dim;
-  const size_t inner = ffa_fwd_workspace_size(&L->inner_shape, static_cast<int32_t>(R2));
-  if (inner == 0) return false;
+  if (check_shape(&L->inner_shape, static_cast<int32_t>(R2)) != FFA_OK) return false;
+  const size_t inner = make_layout(L->inner_shape.total_q, L->inner_shape.total_k, L->inner_shape.num_heads_q,
+                                   L->inner_shape.num_heads_kv, L->inner_shape.head_dim, static_cast<int32_t>(R2),
+                                   /*key_split=*/true)
+                           .fwd_total;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
   const size_t rows = static_cast<size_t>(s->total_q) * s->num_heads_q;
@@ -210,6 +214,7 @@ int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const v
   c.out = wb + L.op; c.lse = reinterpret_cast<float*>(wb + L.lsep);
   c.status = status; c.stream = stream; c.options = options;
   c.alibi_pack = P;
+  c.key_split = true;
   if (page_table != nullptr) {
     c.paged = true;
     c.page_table = page_table; c.page_size = page_size; c.n_pages = n_pages;

@@ -70,9 +70,12 @@ struct FwdSmem {
   static constexpr int kOst = kV + kStages * kTileBytes;
   static constexpr int kOstBytes = kTile * 128;
   static constexpr int kBar = kOst + 2 * kOstBytes;
-  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain,
-  // stall (never arrived on; the failure-detection test waits on it)
-  static constexpr int kNumBars = 2 + 3 * kStages + 8;
+  // q_full, q_empty, k_full[S+1], v_full[S+1], kv_empty[S+1], s_full[2], p_full[2], o_full[2],
+  // drain, stall (never arrived on; the failure-detection test waits on it).  Slot S exists
+  // with the key split only: its K sits in the (then unused) second query tile, its V in the
+  // (then unused) output staging boxes.
+  static constexpr int kNumBars = 2 + 3 * (kStages + 1) + 8;
+  static_assert(kTileBytes <= 2 * kTile * 128, "a V tile fits the two output staging boxes");
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;
@@ -103,6 +106,10 @@ struct FwdParams {
   int* status;
   uint64_t wait_limit_ns;
   int stall;  // failure-detection test: the first wait of every CTA never completes
+  // key split (decode): an item is one query tile of one head; warpgroup w takes the key
+  // tiles w, w + 2, ... of the chunk and writes its own partial result (sub-tile w).  (Last
+  // member: placed earlier, it changed the register allocation of the other kernels.)
+  int key_split;
 };
 
 struct Item {
@@ -113,6 +120,7 @@ struct Item {
 };
 
 // Work item -> (chunk of a group's work list, head slot).  Chunks are taken longest first.
+template <bool kKS>
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int item) {
   Item it;
   const int rank = item / p.slots, slot = item - rank * p.slots;
@@ -122,7 +130,10 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int item) {
   it.pslot = ch.w;
   it.ents = p.plan.grp_ent + static_cast<size_t>(it.g) * p.nkt + ch.y;
   it.slot = slot;
-  if (p.head_pair) {
+  if (kKS) {
+    it.qt0 = it.qt1 = it.g;
+    it.h0 = it.h1 = slot;
+  } else if (p.head_pair) {
     it.qt0 = it.qt1 = it.g;
     it.h0 = 2 * slot;
     it.h1 = 2 * slot + 1;
@@ -272,8 +283,10 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint3
   }
 }
 
-// kFixed: bounded softcap (kCap, no bias, 2 * cap_c <= 120): fixed reference max cap_c
-template <int D, bool kCap, bool kBias, bool kFixed>
+// kFixed: bounded softcap (kCap, no bias, 2 * cap_c <= 120): fixed reference max cap_c.
+// kKS: the key split (FwdParams::key_split), a separate instance so that the other kernels
+// carry none of its bookkeeping
+template <int D, bool kCap, bool kBias, bool kFixed, bool kKS>
 __global__ void __launch_bounds__(kThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -288,9 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
   uint64_t* k_full = bars + 2;
-  uint64_t* v_full = bars + 2 + S;
-  uint64_t* kv_empty = bars + 2 + 2 * S;
-  uint64_t* s_full = bars + 2 + 3 * S;
+  uint64_t* v_full = bars + 2 + (S + 1);
+  uint64_t* kv_empty = bars + 2 + 2 * (S + 1);
+  uint64_t* s_full = bars + 2 + 3 * (S + 1);
   uint64_t* p_full = s_full + 2;
   uint64_t* o_full = s_full + 4;
   uint64_t* drain = s_full + 6;
@@ -302,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s <= S; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -333,6 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
   const int n_items = p.plan.hdr[1] * p.slots;  // chunks x head slots, written by the planner
+  // K/V ring: S slots, one more with the key split (see FwdSmem)
+  constexpr uint32_t nst = kKS ? S + 1 : S;
+  auto k_slot = [&](uint32_t st) {
+    return (kKS && st >= static_cast<uint32_t>(S)) ? static_cast<uint32_t>(SM::kQ1) : SM::kK + st * SM::kTileBytes;
+  };
+  auto v_slot = [&](uint32_t st) {
+    return (kKS && st >= static_cast<uint32_t>(S)) ? static_cast<uint32_t>(SM::kOst) : SM::kV + st * SM::kTileBytes;
+  };
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
@@ -349,18 +370,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int wave = 0; ok; ++wave) {
       const int item = sched_item(wave);
       if (item >= n_items) break;
-      const Item it = decode_item(p, item);
+      const Item it = decode_item<kKS>(p, item);
       const int n = it.n;
       const int qt = wg ? it.qt1 : it.qt0;
       const int h = wg ? it.h1 : it.h0;
       const int row = qt * kTile + r;
       const bool in_rows = row < p.nq;
-      if (n == 0) {
+      // this warpgroup's key tiles: entries j0, j0 + step, ... of the chunk (key split: every
+      // other one, starting at the warpgroup's index)
+      constexpr int step = kKS ? 2 : 1;
+      const int j0 = kKS ? wg : 0;
+      const int n_w = kKS ? (n + 1 - wg) / 2 : n;
+      const int csub = kKS ? 0 : wg;  // which sub-tile's class an entry gives
+      if (n_w == 0) {  // nothing visible here: O = 0, LSE = -inf (a partial result of that value)
         if (in_rows) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
+          if (!kKS) {  // (a chunk of a split row is never empty)
+            uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * p.hq + h) * D);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-          p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
+            for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
+          } else {
+            const size_t prow = (static_cast<size_t>(it.pslot) * p.slots + it.slot) * 2 * kTile + wg * kTile + r;
+            float4* dst = reinterpret_cast<float4*>(p.plan.part_o + prow * D);
+#pragma unroll
+            for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            p.plan.part_lse[prow] = -INFINITY;
+          }
         }
         continue;
       }
@@ -379,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the slice list (rows whose union needs more than two intervals use the list)
       int ilo0, ihi0, ilo1, ihi1;
       const bool ivl_ok = row_intervals(p, row, nsl, sl, ilo0, ihi0, ilo1, ihi1);
-      uint32_t e_next = ents[0];
+      uint32_t e_next = ents[j0];
       // l_run: sum of the fp32 p (for the LSE); r_run: sum of the bf16-rounded p that the PV
       // MMA actually multiplies (normalising O by it keeps the weights a convex combination,
       // so a dominant key is reproduced exactly even when the reference max is stale).  On
@@ -388,11 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // at a fraction of the cost of rounding every p back
       // m_run: the reference max of the exponentials (log2 domain); a bounded softcap fixes it
       float m_run = kFixed ? p.cap_c : -INFINITY, l_run = 0.0f, r_run = 0.0f;
-      for (int j = 0; j < n; ++j) {
+      for (int jj = 0; jj < n_w; ++jj) {
+        const int j = j0 + jj * step;
         const uint32_t e = e_next;
-        if (j + 1 < n) e_next = ents[j + 1];  // in flight while this tile is processed
+        if (jj + 1 < n_w) e_next = ents[j + step];  // in flight while this tile is processed
         const int kt = entry_idx(e);
-        const int cls = entry_cls(e, wg);
+        const int cls = entry_cls(e, csub);
         uint64_t* sb = (p.stall && s_cnt == 0) ? stall_bar : &s_full[wg];
         ok = __all_sync(0xffffffffu, mbar_wait(sb, s_cnt & 1u, abort_flag, lim));
         if (!ok) break;
@@ -746,30 +782,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it_cnt = 0;
       uint32_t gk = 0;
       bool ok = true;
-      int last_use[S];
-      for (int s = 0; s < S; ++s) last_use[s] = -1;
+      int last_use[S + 1];
+      for (int s = 0; s <= S; ++s) last_use[s] = -1;
       int last_q = -1;
       for (int wave = 0; ok; ++wave) {
         const int item = sched_item(wave);
         if (item >= n_items) break;
-        const Item it = decode_item(p, item);
+        const Item it = decode_item<kKS>(p, item);
         const int n = it.n;
         if (n == 0) continue;
         if (it_cnt > 0) {
           ok = mbar_wait(q_empty, (it_cnt - 1) & 1u, abort_flag, lim);
           if (!ok) break;
         }
-        mbar_arrive_expect_tx(q_full, 2 * SM::kTileBytes);
+        mbar_arrive_expect_tx(q_full, (kKS ? 1 : 2) * SM::kTileBytes);
         last_q = static_cast<int>(it_cnt);
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) {
           tma_load_2d(sm + SM::kQ0 + b * SM::kBoxBytes, &tmQ, q_full, it.h0 * D + 64 * b, it.qt0 * kTile);
-          tma_load_2d(sm + SM::kQ1 + b * SM::kBoxBytes, &tmQ, q_full, it.h1 * D + 64 * b, it.qt1 * kTile);
+          if (!kKS)  // (key split: both warpgroups' S use the one query tile)
+            tma_load_2d(sm + SM::kQ1 + b * SM::kBoxBytes, &tmQ, q_full, it.h1 * D + 64 * b, it.qt1 * kTile);
         }
         const uint32_t* ents = it.ents;
         for (int j = 0; j < n; ++j) {
           const int kt = entry_idx(ents[j]);
-          const uint32_t st = gk % S, u = gk / S;
+          const uint32_t st = gk % nst, u = gk / nst;
           if (u > 0) {
             ok = mbar_wait(&kv_empty[st], (u - 1) & 1u, abort_flag, lim);
             if (!ok) break;
@@ -779,11 +816,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.page_table == nullptr) {
 #pragma unroll
             for (int b = 0; b < D / 64; ++b)
-              tma_load_2d(sm + SM::kK + st * SM::kTileBytes + b * SM::kBoxBytes, &tmK, &k_full[st],
+              tma_load_2d(sm + k_slot(st) + b * SM::kBoxBytes, &tmK, &k_full[st],
                           it.kvh * D + 64 * b, kt * kTile);
 #pragma unroll
             for (int b = 0; b < D / 64; ++b)
-              tma_load_2d(sm + SM::kV + st * SM::kTileBytes + b * SM::kBoxBytes, &tmV, &v_full[st],
+              tma_load_2d(sm + v_slot(st) + b * SM::kBoxBytes, &tmV, &v_full[st],
                           it.kvh * D + 64 * b, kt * kTile);
           } else {
             // Paged K/V (FlexAttention paper, section 5, Paged Attention): the tile's 128
@@ -807,9 +844,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t roff = static_cast<uint32_t>(pj * p.page_size) * 128u;
 #pragma unroll
               for (int b = 0; b < D / 64; ++b) {
-                tma_load_2d(sm + SM::kK + st * SM::kTileBytes + b * SM::kBoxBytes + roff, &tmK, &k_full[st],
+                tma_load_2d(sm + k_slot(st) + b * SM::kBoxBytes + roff, &tmK, &k_full[st],
                             it.kvh * D + 64 * b, y);
-                tma_load_2d(sm + SM::kV + st * SM::kTileBytes + b * SM::kBoxBytes + roff, &tmV, &v_full[st],
+                tma_load_2d(sm + v_slot(st) + b * SM::kBoxBytes + roff, &tmV, &v_full[st],
                             it.kvh * D + 64 * b, y);
               }
             }
@@ -824,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // let the copies already issued land before the CTA's shared memory is released
         const uint64_t short_lim = 100000000ull;
         if (last_q >= 0) mbar_wait(q_full, static_cast<uint32_t>(last_q) & 1u, nullptr, short_lim);
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s <= S; ++s) {
           if (last_use[s] < 0) continue;
           mbar_wait(&k_full[s], static_cast<uint32_t>(last_use[s]) & 1u, nullptr, short_lim);
           mbar_wait(&v_full[s], static_cast<uint32_t>(last_use[s]) & 1u, nullptr, short_lim);
@@ -838,55 +875,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, D, false, true);
       const uint32_t sQ0 = smem_u32(sm + SM::kQ0), sQ1 = smem_u32(sm + SM::kQ1);
-      const uint32_t sK = smem_u32(sm + SM::kK), sV = smem_u32(sm + SM::kV);
+      const uint32_t sbase = smem_u32(sm);
       const uint32_t tS0 = tbase, tS1 = tbase + 128, tO0 = tbase + 256, tO1 = tbase + 256 + D;
       uint32_t it_cnt = 0, gk = 0, pc0 = 0, pc1 = 0;
       bool ok = true;
       for (int wave = 0; ok; ++wave) {
         const int item = sched_item(wave);
         if (item >= n_items) break;
-        const Item it = decode_item(p, item);
+        const Item it = decode_item<kKS>(p, item);
         const int n = it.n;
         if (n == 0) continue;
         ok = mbar_wait(q_full, it_cnt & 1u, abort_flag, lim);
         if (!ok) break;
+        if constexpr (kKS) {
+          // warpgroup 0 takes the chunk's key tiles 0, 2, 4, ..., warpgroup 1 the tiles 1, 3,
+          // ...; both multiply the one query tile (Q0).  A tile's K/V slot is released after
+          // its own PV.
+          const int n1 = n / 2, n0 = n - n1;
+          for (int t = 0; t < 2 && t < n; ++t) {  // the first S of each warpgroup
+            const uint32_t g = gk + t, st = g % nst;
+            ok = mbar_wait(&k_full[st], (g / nst) & 1u, abort_flag, lim);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk<D>(t ? tS1 : tS0, sQ0, sbase + k_slot(st), idesc_qk);
+            umma_commit(&s_full[t]);
+            if (t == n - 1) umma_commit(q_empty);
+          }
+          for (int i = 0; i < n0 && ok; ++i) {
+            for (int w = 0; w < 2; ++w) {
+              const int jt = 2 * i + w;  // warpgroup w's i-th tile
+              if (jt >= n) break;
+              const uint32_t g = gk + jt, st = g % nst;
+              uint32_t& pc = w ? pc1 : pc0;
+              ok = mbar_wait(&v_full[st], (g / nst) & 1u, abort_flag, lim) &&
+                   mbar_wait(&p_full[w], pc & 1u, abort_flag, lim);
+              if (!ok) break;
+              ++pc;
+              tc_fence_after();
+              issue_pv<D>(w ? tO1 : tO0, w ? tS1 : tS0, sbase + v_slot(st), idesc_pv, i > 0);
+              umma_commit(&kv_empty[st]);
+              if (i == (w ? n1 : n0) - 1) umma_commit(&o_full[w]);
+              const int jn = jt + 2;  // the warpgroup's next tile
+              if (jn < n) {
+                const uint32_t g2 = gk + jn, st2 = g2 % nst;
+                ok = mbar_wait(&k_full[st2], (g2 / nst) & 1u, abort_flag, lim);
+                if (!ok) break;
+                tc_fence_after();
+                issue_qk<D>(w ? tS1 : tS0, sQ0, sbase + k_slot(st2), idesc_qk);
+                umma_commit(&s_full[w]);
+                if (jn == n - 1) umma_commit(q_empty);
+              }
+            }
+          }
+          gk += n;
+          ++it_cnt;
+          continue;
+        }
         {
-          const uint32_t st = gk % S;
-          ok = mbar_wait(&k_full[st], (gk / S) & 1u, abort_flag, lim);
+          const uint32_t st = gk % nst;
+          ok = mbar_wait(&k_full[st], (gk / nst) & 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
-          issue_qk<D>(tS0, sQ0, sK + st * SM::kTileBytes, idesc_qk);
+          issue_qk<D>(tS0, sQ0, sbase + k_slot(st), idesc_qk);
           umma_commit(&s_full[0]);
-          issue_qk<D>(tS1, sQ1, sK + st * SM::kTileBytes, idesc_qk);
+          issue_qk<D>(tS1, sQ1, sbase + k_slot(st), idesc_qk);
           umma_commit(&s_full[1]);
           if (n == 1) umma_commit(q_empty);
         }
         for (int j = 0; j < n && ok; ++j) {
-          const uint32_t g = gk + j, st = g % S;
-          ok = mbar_wait(&v_full[st], (g / S) & 1u, abort_flag, lim) &&
+          const uint32_t g = gk + j, st = g % nst;
+          ok = mbar_wait(&v_full[st], (g / nst) & 1u, abort_flag, lim) &&
                mbar_wait(&p_full[0], pc0 & 1u, abort_flag, lim);
           if (!ok) break;
           ++pc0;
           tc_fence_after();
-          issue_pv<D>(tO0, tS0, sV + st * SM::kTileBytes, idesc_pv, j > 0);
+          issue_pv<D>(tO0, tS0, sbase + v_slot(st), idesc_pv, j > 0);
           if (j == n - 1) umma_commit(&o_full[0]);
-          const uint32_t g1 = g + 1, st1 = g1 % S;
+          const uint32_t g1 = g + 1, st1 = g1 % nst;
           if (j + 1 < n) {
-            ok = mbar_wait(&k_full[st1], (g1 / S) & 1u, abort_flag, lim);
+            ok = mbar_wait(&k_full[st1], (g1 / nst) & 1u, abort_flag, lim);
             if (!ok) break;
             tc_fence_after();
-            issue_qk<D>(tS0, sQ0, sK + st1 * SM::kTileBytes, idesc_qk);
+            issue_qk<D>(tS0, sQ0, sbase + k_slot(st1), idesc_qk);
             umma_commit(&s_full[0]);
           }
           ok = mbar_wait(&p_full[1], pc1 & 1u, abort_flag, lim);
           if (!ok) break;
           ++pc1;
           tc_fence_after();
-          issue_pv<D>(tO1, tS1, sV + st * SM::kTileBytes, idesc_pv, j > 0);
+          issue_pv<D>(tO1, tS1, sbase + v_slot(st), idesc_pv, j > 0);
           umma_commit(&kv_empty[st]);
           if (j == n - 1) umma_commit(&o_full[1]);
           if (j + 1 < n) {
-            issue_qk<D>(tS1, sQ1, sK + st1 * SM::kTileBytes, idesc_qk);
+            issue_qk<D>(tS1, sQ1, sbase + k_slot(st1), idesc_qk);
             umma_commit(&s_full[1]);
             if (j + 2 == n) umma_commit(q_empty);
           }
@@ -914,10 +995,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // LSE merge of split rows: for a group whose work list was cut into chunks, every row combines
 // its chunks' partial results, L = log sum_c e^{L_c} and O = sum_c e^{L_c - L} O_c (the
 // chunks cover disjoint key sets of the row); rows whose chunks all have L_c = -inf get
-// O = 0 and L = -inf.  One block per (group, head slot, sub-tile, row): its eight warps take
-// every eighth chunk, a lane holds D / 32 columns (coalesced loads of a partial row), and the
-// warps' sums are combined in shared memory.  Rows past the end return at once.
-constexpr int kMergeWarps = 8;
+// O = 0 and L = -inf.  One block per (group, head slot, sub-tile, row) — with the key split,
+// per (query tile, head, row), over both warpgroups' partials of every chunk: its sixteen warps
+// take every sixteenth partial, a lane holds D / 32 columns (coalesced loads of a partial row),
+// and the warps' sums are combined in shared memory.  Rows past the end return at once.
+constexpr int kMergeWarps = 16;
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParams p) {
   constexpr int kPer = D / 32;  // columns per lane
@@ -927,13 +1009,19 @@ __global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParam
   int b = blockIdx.x;
   const int r = b % kTile;
   b /= kTile;
-  const int sub = b & 1;
-  b >>= 1;
+  // key split: one block per row, merging both warpgroups' partials of every chunk
+  const int sub = p.key_split ? 0 : (b & 1);
+  if (!p.key_split) b >>= 1;
   const int g = b / p.slots, slot = b - (b / p.slots) * p.slots;
   const int nch = p.plan.grp_nch[g];
-  if (nch <= 1) return;
+  if (!p.key_split && nch <= 1) return;
+  const int nsub = p.key_split ? 2 : 1;
+  const int npart = nch * nsub;  // partial results of this row
   int qt, h;
-  if (p.head_pair) {
+  if (p.key_split) {
+    qt = g;
+    h = slot;
+  } else if (p.head_pair) {
     qt = g;
     h = 2 * slot + sub;
   } else {
@@ -944,10 +1032,13 @@ __global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParam
   if (row >= p.nq) return;
   const int ps = p.plan.grp_pslot[g];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  auto prow = [&](int c) { return (static_cast<size_t>(ps + c) * p.slots + slot) * 2 * kTile + sub * kTile + r; };
-  // the largest chunk LSE
+  // partial k: chunk k / nsub, sub-tile (key split: warpgroup) k % nsub
+  auto prow = [&](int k) {
+    return (static_cast<size_t>(ps + k / nsub) * p.slots + slot) * 2 * kTile + (sub + k % nsub) * kTile + r;
+  };
+  // the largest partial LSE
   float mx = -INFINITY;
-  for (int c = threadIdx.x; c < nch; c += blockDim.x) mx = fmaxf(mx, p.plan.part_lse[prow(c)]);
+  for (int c = threadIdx.x; c < npart; c += blockDim.x) mx = fmaxf(mx, p.plan.part_lse[prow(c)]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) sh_max[warp] = mx;
@@ -969,7 +1060,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParam
   for (int k = 0; k < kPer; ++k) acc[k] = 0.0f;
   float wsum = 0.0f;
 #pragma unroll 4
-  for (int c = warp; c < nch; c += kMergeWarps) {
+  for (int c = warp; c < npart; c += kMergeWarps) {
     const size_t pr = prow(c);
     const float w = ex2_approx((p.plan.part_lse[pr] - mx) * kLog2e);
     wsum += w;
@@ -1009,10 +1100,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParam
   }
 }
 
-template <int D, bool kCap, bool kBias, bool kFixed>
+template <int D, bool kCap, bool kBias, bool kFixed, bool kKS>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   using SM = FwdSmem<D>;
-  auto kern = ffa_fwd_kernel<D, kCap, kBias, kFixed>;
+  auto kern = ffa_fwd_kernel<D, kCap, kBias, kFixed, kKS>;
   // Once per device (the shared-memory attribute applies to the device current when it is
   // set).  The register split (setmaxnreg) is balanced for exactly kRegsLaunch registers per
   // thread at launch; with any other count a softmax warp's increase could never be granted,
@@ -1044,6 +1135,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.nq = P.nq; p.nk = P.nk; p.hq = P.hq; p.hkv = P.hkv; p.G = P.hq / P.hkv;
   p.nqt = P.nqt; p.nkt = P.nkt;
   p.head_pair = a.head_pair; p.slots = a.slots;
+  p.key_split = a.key_split;
   p.scale_log2 = a.scale * kLog2e;
   p.cap_c = a.softcap * kLog2e;
   p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
@@ -1068,24 +1160,29 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   if (g_kernel_events.fwd_stop != nullptr) cudaEventRecord(g_kernel_events.fwd_stop, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !a.split) return e;
-  ffa_fwd_merge<D><<<a.ngrp * a.slots * 2 * kTile, 32 * kMergeWarps, 0, stream>>>(p);
+  ffa_fwd_merge<D><<<a.ngrp * a.slots * (a.key_split ? 1 : 2) * kTile, 32 * kMergeWarps, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <bool kKS>
+cudaError_t launch_variant(const FwdArgs& a, cudaStream_t s) {
+  const bool cap = a.softcap > 0.0f, bias = a.alibi != nullptr;
+  // a bounded softcap without ALiBi takes the fixed-reference kernel (FwdParams::cap_fixed)
+  const bool fixed = cap && !bias && 2.0f * a.softcap * kLog2e <= 120.0f;
+  if (a.P.d == 64) {
+    if (bias) return cap ? launch_impl<64, true, true, false, kKS>(a, s) : launch_impl<64, false, true, false, kKS>(a, s);
+    if (fixed) return launch_impl<64, true, false, true, kKS>(a, s);
+    return cap ? launch_impl<64, true, false, false, kKS>(a, s) : launch_impl<64, false, false, false, kKS>(a, s);
+  }
+  if (bias) return cap ? launch_impl<128, true, true, false, kKS>(a, s) : launch_impl<128, false, true, false, kKS>(a, s);
+  if (fixed) return launch_impl<128, true, false, true, kKS>(a, s);
+  return cap ? launch_impl<128, true, false, false, kKS>(a, s) : launch_impl<128, false, false, false, kKS>(a, s);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
-  const bool cap = a.softcap > 0.0f, bias = a.alibi != nullptr;
-  // a bounded softcap without ALiBi takes the fixed-reference kernel (FwdParams::cap_fixed)
-  const bool fixed = cap && !bias && 2.0f * a.softcap * kLog2e <= 120.0f;
-  if (a.P.d == 64) {
-    if (bias) return cap ? launch_impl<64, true, true, false>(a, s) : launch_impl<64, false, true, false>(a, s);
-    if (fixed) return launch_impl<64, true, false, true>(a, s);
-    return cap ? launch_impl<64, true, false, false>(a, s) : launch_impl<64, false, false, false>(a, s);
-  }
-  if (bias) return cap ? launch_impl<128, true, true, false>(a, s) : launch_impl<128, false, true, false>(a, s);
-  if (fixed) return launch_impl<128, true, false, true>(a, s);
-  return cap ? launch_impl<128, true, false, false>(a, s) : launch_impl<128, false, false, false>(a, s);
+  return a.key_split ? launch_variant<true>(a, s) : launch_variant<false>(a, s);
 }
 
 }  // namespace ffa

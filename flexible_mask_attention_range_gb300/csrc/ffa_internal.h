@@ -38,6 +38,9 @@ struct WsLayout {
   int hq = 0, hkv = 0, d = 0, R = 0;
   int nqt = 0, nkt = 0;
   bool head_pair = true;  // forward pairs two query heads of one KV group (else two q-tiles)
+  // forward key split (decode): an item is one query tile of one head; its two softmax
+  // warpgroups take alternate key tiles and write two partial results for the merge
+  bool key_split = false;
   int ngrp = 0, slots = 0;
   int split_len = 0;      // key tiles per forward chunk (>= nkt: no row is split)
   int nch_max = 1;        // most chunks one group can have
@@ -81,21 +84,27 @@ inline void fold_cap_poly(float scale, float softcap, float (&q_out)[4], float* 
   *slim = s;
 }
 
-inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int R) {
+inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int R, bool key_split = false) {
   WsLayout L;
   L.nq = nq; L.nk = nk; L.hq = hq; L.hkv = hkv; L.d = d; L.R = R;
   L.nqt = static_cast<int>((nq + kTile - 1) / kTile);
   L.nkt = static_cast<int>((nk + kTile - 1) / kTile);
   const int G = hkv > 0 ? hq / hkv : 1;
-  L.head_pair = (G % 2 == 0);
-  L.ngrp = L.head_pair ? L.nqt : (L.nqt + 1) / 2;
+  L.key_split = key_split;
+  L.head_pair = !key_split && (G % 2 == 0);
+  L.ngrp = (L.head_pair || key_split) ? L.nqt : (L.nqt + 1) / 2;
   L.slots = L.head_pair ? hq / 2 : hq;
   {
     const int64_t items = static_cast<int64_t>(L.ngrp) * L.slots;
     L.split_len = L.nkt > 0 ? L.nkt : 1;
-    if (items > 0 && items < kSplitTarget / 2 && L.nkt >= kMinSplitTiles) {
-      const int64_t splits = (kSplitTarget + items - 1) / items;
-      int64_t len = (L.nkt + splits - 1) / splits;
+    // The key split's items run both warpgroups on one chunk, so half as many chunks fill the
+    // GPU; its rows (decoding: every query tile holds its own tokens' sequences) see about
+    // nkt / nqt key tiles each, which is what the chunk length is cut from
+    const int64_t target = key_split ? kSplitTarget / 2 : kSplitTarget;
+    const int64_t row_len = key_split && L.nqt > 0 ? (L.nkt + L.nqt - 1) / L.nqt : L.nkt;
+    if (items > 0 && items < target && L.nkt >= kMinSplitTiles) {
+      const int64_t splits = (target + items - 1) / items;
+      int64_t len = (row_len + splits - 1) / splits;
       if (len < kMinChunk) len = kMinChunk;
       if (len < L.nkt) {
         L.split_len = static_cast<int>(len);
@@ -104,6 +113,7 @@ inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int 
     }
     L.nch_max = (L.nkt + L.split_len - 1) / L.split_len;
     if (L.nch_max < 1) L.nch_max = 1;
+    if (key_split) L.split = true;  // every item leaves two partial results
   }
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
@@ -213,6 +223,7 @@ struct FwdArgs {
   ProblemDims P;
   int head_pair, ngrp, slots, n_items;  // n_items: upper bound (chunks x slots) for the grid
   int split;
+  int key_split = 0;  // WsLayout::key_split
   float scale, softcap;
   const void *q, *k, *v;
   void* out;
@@ -273,7 +284,10 @@ struct FwdCall {
   int page_size = 0;
   int64_t n_pages = 0;
   int alibi_pack = 0;  // > 0: rows are packed (token, query head) pairs (decode), see FwdArgs
+  bool key_split = false;  // WsLayout::key_split (decode)
 };
+// Shape check shared by the entry points (FFA_OK or the error code).
+int check_shape(const ffa_shape* s, int32_t n_ranges);
 // Options check shared by the entry points: reserved fields zero, slopes 4-byte aligned.
 int check_options(const ffa_options* o);
 // Host-detectable errors of a forward call (nothing is launched); fills the workspace layout.

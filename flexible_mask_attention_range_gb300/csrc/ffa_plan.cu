@@ -208,7 +208,10 @@ __global__ void __launch_bounds__(256) plan_row_classes_kernel(ProblemDims P, Pl
 
 // Work lists: one block per forward group.  head_pair: the group is one query tile; otherwise
 // it is the query-tile pair (2g, 2g+1) whose work list is the union of both rows.  Entries:
-// key tiles non-empty for either sub-tile, ascending, with both sub-tiles' classes.
+// key tiles non-empty for either sub-tile, ascending, with both sub-tiles' classes.  A thread
+// takes kListRun consecutive key tiles per pass, so a row of thousands of key tiles (a
+// decoding batch) needs few block-wide scans.
+constexpr int kListRun = 16;
 __global__ void __launch_bounds__(256) plan_row_lists_kernel(ProblemDims P, int head_pair, PlanView v) {
   __shared__ int warp_buf[32];
   const int g = blockIdx.x;
@@ -216,17 +219,22 @@ __global__ void __launch_bounds__(256) plan_row_lists_kernel(ProblemDims P, int 
   const uint8_t* ca_row = v.cls + static_cast<size_t>(qa) * P.nkt;
   const uint8_t* cb_row = qb < P.nqt ? v.cls + static_cast<size_t>(qb) * P.nkt : nullptr;
   int count = 0;
-  for (int c = 0; c < P.nkt; c += blockDim.x) {
-    const int kt = c + threadIdx.x;
-    int ca = 0, cb = 0;
-    if (kt < P.nkt) {
-      ca = ca_row[kt];
-      cb = head_pair ? ca : (cb_row != nullptr ? cb_row[kt] : FFA_TILE_EMPTY);
+  for (int c = 0; c < P.nkt; c += blockDim.x * kListRun) {
+    const int kt0 = c + threadIdx.x * kListRun;
+    uint8_t ca[kListRun], cb[kListRun];
+    int n_keep = 0;
+#pragma unroll
+    for (int i = 0; i < kListRun; ++i) {
+      const int kt = kt0 + i;
+      ca[i] = kt < P.nkt ? ca_row[kt] : static_cast<uint8_t>(FFA_TILE_EMPTY);
+      cb[i] = head_pair ? ca[i] : (cb_row != nullptr && kt < P.nkt ? cb_row[kt] : static_cast<uint8_t>(FFA_TILE_EMPTY));
+      n_keep += (ca[i] | cb[i]) != 0;
     }
-    const int keep = (ca | cb) != 0;
     int total;
-    const int pos = count + block_exclusive_scan(keep, warp_buf, &total);
-    if (keep) v.grp_ent[static_cast<size_t>(g) * P.nkt + pos] = make_entry(kt, ca, cb);
+    int pos = count + block_exclusive_scan(n_keep, warp_buf, &total);
+#pragma unroll
+    for (int i = 0; i < kListRun; ++i)
+      if ((ca[i] | cb[i]) != 0) v.grp_ent[static_cast<size_t>(g) * P.nkt + pos++] = make_entry(kt0 + i, ca[i], cb[i]);
     count += total;
   }
   if (threadIdx.x == 0) v.grp_cnt[g] = count;
@@ -295,7 +303,9 @@ __device__ void counting_sort_desc(const int* __restrict__ len, int n, int max_l
   for (int base = 0; base < n; base += blockDim.x) {
     const int i = base + threadIdx.x;
     const int c = i < n ? min(max(len[i], 0), max_len) : -1;
-    for (int ww = 0; ww < nw; ++ww) {
+    // only the warps that hold items of this pass take turns
+    const int nw_pass = min(nw, (n - base + 31) >> 5);
+    for (int ww = 0; ww < nw_pass; ++ww) {
       if (w == ww) {
         const unsigned peers = __match_any_sync(0xffffffffu, c);
         const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -323,9 +333,10 @@ __global__ void __launch_bounds__(1024) plan_order_kernel(const int* __restrict_
 
 // ---------------------------------------------------------------- 3'. forward chunks
 // One block.  Cuts every group's work list into chunks of at most `split_len` entries (one
-// chunk, possibly empty, when the list is short), gives the chunks of split groups
-// consecutive partial-output slots, and orders all chunks longest first.  hdr[1] = chunks.
-__global__ void __launch_bounds__(1024) plan_chunks_kernel(int ngrp, int split_len, PlanView v) {
+// chunk, possibly empty, when the list is short), gives the chunks of split groups (every
+// group when `all_split`: the key-split forward) consecutive partial-output slots, and orders
+// all chunks longest first.  hdr[1] = chunks.
+__global__ void __launch_bounds__(1024) plan_chunks_kernel(int ngrp, int split_len, int all_split, PlanView v) {
   extern __shared__ int hist[];  // split_len + 1
   __shared__ int warp_buf[32];
   int base = 0, pbase = 0;
@@ -336,7 +347,7 @@ __global__ void __launch_bounds__(1024) plan_chunks_kernel(int ngrp, int split_l
       cnt = v.grp_cnt[g];
       nch = max(1, (cnt + split_len - 1) / split_len);
     }
-    const bool split = nch > 1;
+    const bool split = nch > 1 || (all_split && g < ngrp);
     int total, ptotal;
     const int pos = base + block_exclusive_scan(nch, warp_buf, &total);
     const int ppos = pbase + block_exclusive_scan(split ? nch : 0, warp_buf, &ptotal);
@@ -392,11 +403,12 @@ cudaError_t launch_plan_rows(const ProblemDims& P, const WsLayout& L, const Plan
   plan_row_classes_kernel<<<dim3(P.nqt, (P.nkt + kPlanSpan - 1) / kPlanSpan), 256, 0, s>>>(P, v);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  plan_row_lists_kernel<<<L.ngrp, 256, 0, s>>>(P, L.head_pair ? 1 : 0, v);
+  // a key-split group is one query tile, as a head pair's is
+  plan_row_lists_kernel<<<L.ngrp, 256, 0, s>>>(P, (L.head_pair || L.key_split) ? 1 : 0, v);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem = static_cast<size_t>(L.split_len + 1) * sizeof(int);
-  plan_chunks_kernel<<<1, 1024, smem, s>>>(L.ngrp, L.split_len, v);
+  plan_chunks_kernel<<<1, 1024, smem, s>>>(L.ngrp, L.split_len, L.key_split ? 1 : 0, v);
   return cudaGetLastError();
 }
 

@@ -212,9 +212,10 @@ int ffa_fwd_paged(const ffa_shape* shape, const void* q, const void* k_pages, co
  *   max_seqlen_q  >= 1: the most query tokens any CAUSAL slice has (the max_seqlen_q
  *                 argument of flex_flash_attn_func); a CAUSAL slice with more is dropped and
  *                 reported with FFA_STATUS_BAD_RANGE
- * The query heads of every token are processed as rows of the key/value head they share
- * (G / 2 rows per packed head when G = Hq / Hkv is even, G otherwise), so each key tile is
- * read once per key/value head instead of once per pair of query heads.  options->alibi_slopes
+ * The G = Hq / Hkv query heads of every token are processed as G rows of the key/value head
+ * they share, so each key tile is read once per (128-row query tile, key/value head) and
+ * multiplied once, by alternating halves of the work item (the forward pass's key split).
+ * options->alibi_slopes
  * ([Hq], as for ffa_fwd_ex) gives every query head its own slope and every token its own
  * position, exactly as in the unpacked problem.  Requires total_q * G <= FFA_MAX_TOKENS.
  * workspace: ffa_fwd_decode_workspace_size() bytes.
