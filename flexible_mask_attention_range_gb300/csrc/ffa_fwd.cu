@@ -110,6 +110,7 @@ struct FwdParams {
   // tiles w, w + 2, ... of the chunk and writes its own partial result (sub-tile w).  (Last
   // member: placed earlier, it changed the register allocation of the other kernels.)
   int key_split;
+  float cap_q5[3];  // cap_q in degree 5 (kTanhPoly5): the bounded-softcap kernel's form
 };
 
 struct Item {
@@ -493,8 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 nm2 = make_float2(-p.cap_c, -p.cap_c);
           auto exp_fixed = [&](auto poly_tag, auto mask_tag) {
             constexpr bool kP = decltype(poly_tag)::value, kM = decltype(mask_tag)::value;
-            const float2 q0 = make_float2(p.cap_q[0], p.cap_q[0]), q1 = make_float2(p.cap_q[1], p.cap_q[1]);
-            const float2 q2 = make_float2(p.cap_q[2], p.cap_q[2]), q3 = make_float2(p.cap_q[3], p.cap_q[3]);
+            // the degree-5 polynomial (four packed instructions per pair of scores)
+            const float2 q0 = make_float2(p.cap_q5[0], p.cap_q5[0]), q1 = make_float2(p.cap_q5[1], p.cap_q5[1]);
+            const float2 q2 = make_float2(p.cap_q5[2], p.cap_q5[2]);
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
               uint32_t pk[16];
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float2 y;
                 if constexpr (kP) {
                   const float2 t = mul2(s2, s2);
-                  y = fma2(s2, fma2(fma2(fma2(q3, t, q2), t, q1), t, q0), nm2);
+                  y = fma2(s2, fma2(fma2(q2, t, q1), t, q0), nm2);
                 } else {
                   y = add2(s2, nm2);
                 }
@@ -544,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // error of the tile's largest p (the only one that can dominate a row), recomputed
             // with the exponential pass's exact operations
             const float t = smax * smax;
-            const float y_max = poly_f ? fmaf(smax, fmaf(fmaf(fmaf(p.cap_q[3], t, p.cap_q[2]), t, p.cap_q[1]), t, p.cap_q[0]), -p.cap_c)
+            const float y_max = poly_f ? fmaf(smax, fmaf(fmaf(p.cap_q5[2], t, p.cap_q5[1]), t, p.cap_q5[0]), -p.cap_c)
                                        : capped_log2(smax, p.cap_c, p.cap_k) + (-p.cap_c);
             const float p_max = ex2_approx(y_max);
             r_run += tile_l + (__uint_as_float(pack_bf16x2(p_max, 0.0f) << 16) - p_max);
@@ -1140,6 +1142,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.cap_c = a.softcap * kLog2e;
   p.cap_k = a.softcap > 0.0f ? 2.0f * a.scale * kLog2e / a.softcap : 0.0f;
   fold_cap_poly(a.scale, a.softcap, p.cap_q, &p.cap_slim);
+  fold_cap_poly5(a.scale, a.softcap, p.cap_q5);
   p.cap_fixed = (a.softcap > 0.0f && 2.0f * p.cap_c <= 120.0f) ? 1 : 0;
   p.plan = a.plan;
   p.out = static_cast<__nv_bfloat16*>(a.out);

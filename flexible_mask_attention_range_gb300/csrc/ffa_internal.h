@@ -62,6 +62,11 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // y * P(y^2) stays within 1.6e-7 of tanh(y), relative, over the whole interval.
 constexpr double kTanhPolyY = 0.375;
 constexpr double kTanhPoly[4] = {9.999999405e-01, -3.333197486e-01, 1.328450275e-01, -4.827228855e-02};
+// Degree 5 (tanh(y) / y ~ c0 + c1 y^2 + c2 y^4 on the same interval, same fit): within 4.5e-6
+// of tanh(y), relative.  The bounded-softcap forward kernel (softcap * log2(e) <= 60) uses it:
+// there the capped logit's error stays below 4.5e-6 * 60 * tanh(0.375) < 1e-4 in the log2
+// domain, a relative error of p below 7e-5, far inside the bf16 rounding of P (2^-9).
+constexpr double kTanhPoly5[3] = {9.999957083e-01, -3.327806792e-01, 1.226476579e-01};
 
 // The capped logit in the log2 domain, x(s) = C tanh(a s) with a = scale / softcap and
 // C = softcap * log2(e), folded into one odd polynomial of the raw score:
@@ -82,6 +87,15 @@ inline void fold_cap_poly(float scale, float softcap, float (&q_out)[4], float* 
   if (!std::isfinite(s) || !std::isfinite(s * s)) return;
   for (int i = 0; i < 4; ++i) q_out[i] = q[i];
   *slim = s;
+}
+
+// The degree-5 form of fold_cap_poly (kTanhPoly5), same interval and *slim.
+inline void fold_cap_poly5(float scale, float softcap, float (&q_out)[3]) {
+  for (int i = 0; i < 3; ++i) q_out[i] = 0.0f;
+  if (!(softcap > 0.0f) || !(scale > 0.0f)) return;
+  const double a = static_cast<double>(scale) / softcap;
+  const double C = static_cast<double>(softcap) * 1.4426950408889634;
+  for (int i = 0; i < 3; ++i) q_out[i] = static_cast<float>(C * kTanhPoly5[i] * std::pow(a, 2 * i + 1));
 }
 
 inline WsLayout make_layout(int64_t nq, int64_t nk, int hq, int hkv, int d, int R, bool key_split = false) {

@@ -1,10 +1,13 @@
-"""Fit the softcap polynomial used by the kernels (kTanhPoly in csrc/ffa_internal.h).
+"""Fit the softcap polynomials used by the kernels (kTanhPoly and kTanhPoly5 in
+csrc/ffa_internal.h).
 
 The kernels form the capped logit softcap * tanh(y), y = scale * q.k / softcap, on tiles
-whose scores all satisfy |y| <= Y = 0.375 with an odd polynomial y * P(y^2),
-P(t) = c0 + c1 t + c2 t^2 + c3 t^3, on the FMA pipe instead of the exponential and
-reciprocal a direct evaluation needs.  This script finds c0..c3 that minimise the largest
-relative error |y P(y^2) - tanh(y)| / |tanh(y)| over (0, Y]:
+whose scores all satisfy |y| <= Y = 0.375 with an odd polynomial y * P(y^2) on the FMA pipe
+instead of the exponential and reciprocal a direct evaluation needs: P(t) = c0 + c1 t +
+c2 t^2 + c3 t^3 (kTanhPoly, degree 7 in y), or, in the bounded-softcap forward kernel,
+P(t) = c0 + c1 t + c2 t^2 (kTanhPoly5, degree 5: one instruction less per pair of scores).
+This script finds the coefficients that minimise the largest relative error
+|y P(y^2) - tanh(y)| / |tanh(y)| over (0, Y]:
 
   * start from a least-squares fit of tanh(y)/y on Chebyshev nodes of (0, Y];
   * reweight the nodes by their current error and refit (Lawson's algorithm for the
@@ -19,16 +22,16 @@ from __future__ import annotations
 import numpy as np
 
 Y = 0.375
-DEGREE = 4  # coefficients of P (in t = y^2)
+DEGREE = 4  # coefficients of P (in t = y^2) for kTanhPoly; kTanhPoly5 has 3
 
 
-def fit(nodes: int = 400, iters: int = 2000) -> np.ndarray:
+def fit(nodes: int = 400, iters: int = 2000, degree: int = DEGREE) -> np.ndarray:
     k = np.arange(nodes)
     y = 0.5 * Y * (1.0 - np.cos(np.pi * (k + 0.5) / nodes))  # Chebyshev nodes on (0, Y)
     target = np.tanh(y) / y
-    A = np.stack([(y * y) ** i for i in range(DEGREE)], axis=1)
+    A = np.stack([(y * y) ** i for i in range(degree)], axis=1)
     w = np.full(nodes, 1.0 / nodes)
-    c = np.zeros(DEGREE)
+    c = np.zeros(degree)
     for _ in range(iters):
         sw = np.sqrt(w)
         # relative error of y P(y^2) against tanh(y) equals that of P against tanh(y)/y
@@ -47,17 +50,18 @@ def max_rel_err_f32(c: np.ndarray, n: int = 200001) -> float:
     yf = y.astype(np.float32)
     t = yf * yf
     cf = c.astype(np.float32)
-    p = cf[3]
-    for i in (2, 1, 0):
+    p = cf[-1]
+    for i in range(len(cf) - 2, -1, -1):
         p = p * t + cf[i]
     approx = (yf * p).astype(np.float64)
     return float(np.max(np.abs(approx - np.tanh(y)) / np.tanh(y)))
 
 
 def main() -> None:
-    c = fit()
-    print("kTanhPoly = {" + ", ".join(f"{x:.9e}" for x in c) + "}")
-    print(f"max relative error (float32 Horner) on (0, {Y}]: {max_rel_err_f32(c):.3e}")
+    for name, degree in (("kTanhPoly", DEGREE), ("kTanhPoly5", 3)):
+        c = fit(degree=degree)
+        print(name + " = {" + ", ".join(f"{x:.9e}" for x in c) + "}")
+        print(f"  max relative error (float32 Horner) on (0, {Y}]: {max_rel_err_f32(c):.3e}")
 
 
 if __name__ == "__main__":
