@@ -174,9 +174,11 @@ int fwd_launch(const FwdCall& c, const WsLayout& L, void* scratch) {
   const int64_t nq = shape->total_q, nk = shape->total_k;
   cudaStream_t s = static_cast<cudaStream_t>(c.stream);
   const int d = shape->head_dim, hq = shape->num_heads_q;
-  if (nk == 0) {  // no key at all: every row is empty
-    if (cudaMemsetAsync(c.out, 0, static_cast<size_t>(nq) * hq * d * 2, s) != cudaSuccess) return FFA_ERR_CUDA;
-    fill_empty_fwd_kernel<<<256, 256, 0, s>>>(c.lse, static_cast<size_t>(nq) * hq);
+  if (nk == 0) {  // no key at all: every row is empty (the unpacked layout has the same sizes)
+    void* o = c.unpack_out != nullptr ? c.unpack_out : c.out;
+    float* l = c.unpack_lse != nullptr ? c.unpack_lse : c.lse;
+    if (cudaMemsetAsync(o, 0, static_cast<size_t>(nq) * hq * d * 2, s) != cudaSuccess) return FFA_ERR_CUDA;
+    fill_empty_fwd_kernel<<<256, 256, 0, s>>>(l, static_cast<size_t>(nq) * hq);
     return cuda_status(cudaGetLastError());
   }
   const ProblemDims P = dims_of(L);
@@ -192,6 +194,10 @@ int fwd_launch(const FwdCall& c, const WsLayout& L, void* scratch) {
   a.n_items = L.ngrp * L.nch_max * L.slots;
   a.split = L.split ? 1 : 0;
   a.key_split = L.key_split ? 1 : 0;
+  if (L.key_split) {
+    a.unpack_out = c.unpack_out;
+    a.unpack_lse = c.unpack_lse;
+  }
   a.scale = resolve_scale(c.softmax_scale, d);
   a.softcap = c.softcap;
   a.q = c.q;

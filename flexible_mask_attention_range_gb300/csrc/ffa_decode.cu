@@ -21,8 +21,8 @@
 // slices, one per token i, over the keys that token sees under the bottom-right alignment
 // used everywhere in this library (j <= i + ke - qe).  max_seqlen_q bounds m, so the
 // rewritten list has a fixed length n_ranges * max_seqlen_q (unused entries are empty
-// slices).  Packing, rewriting and unpacking are three small kernels around the forward pass
-// (dense or paged).  With ALiBi (FlexAttention paper, sections 2 and 3.1; decoding with GQA
+// slices).  Packing and rewriting are two small kernels before the forward pass (dense or
+// paged); the forward pass's LSE merge writes O and LSE in the caller's layout.  With ALiBi (FlexAttention paper, sections 2 and 3.1; decoding with GQA
 // and ALiBi is one of the cases its section 6 measures) a packed row keeps the slope of its
 // query head and the position of its token, so the bias is the one of the unpacked problem.
 #include <cstdint>
@@ -45,27 +45,6 @@ __global__ void __launch_bounds__(256) decode_pack_q(const uint4* __restrict__ q
     const int64_t h = row % hp, ig = row / hp;
     const int64_t g = ig % P, i = ig / P;
     qp[idx] = q[(i * hq + h * P + g) * per_row + c];
-  }
-}
-
-// op [N * P, Hq / P, d] -> out [N, Hq, d]; lsep [Hq / P, N * P] -> lse [Hq, N].
-__global__ void __launch_bounds__(256) decode_unpack(const uint4* __restrict__ op, uint4* __restrict__ out,
-                                                     const float* __restrict__ lsep, float* __restrict__ lse,
-                                                     int64_t n, int hq, int P, int d) {
-  const int hp = hq / P;
-  const int64_t per_row = d / 8;
-  const int64_t total = n * hq * per_row;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total; idx += stride) {
-    const int64_t row = idx / per_row, c = idx - row * per_row;  // out row = i * hq + head
-    const int64_t head = row % hq, i = row / hq;
-    const int64_t h = head / P, g = head - h * P;
-    out[idx] = op[((i * P + g) * hp + h) * per_row + c];
-  }
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n * hq; idx += stride) {
-    const int64_t head = idx / n, i = idx - head * n;
-    const int64_t h = head / P, g = head - h * P;
-    lse[idx] = lsep[h * (n * P) + i * P + g];
   }
 }
 
@@ -111,7 +90,7 @@ __global__ void __launch_bounds__(256) decode_slices(const int32_t* __restrict__
 int pack_factor(int G) { return G; }
 
 struct DecodeLayout {
-  size_t qp = 0, op = 0, lsep = 0, qr2 = 0, kr2 = 0, ty2 = 0, inner = 0, total = 0;
+  size_t qp = 0, qr2 = 0, kr2 = 0, ty2 = 0, inner = 0, total = 0;
   int64_t R2 = 0;
   int P = 1;
   ffa_shape inner_shape{};
@@ -140,8 +119,6 @@ bool decode_layout(const ffa_shape* s, int32_t n_ranges, int32_t max_seqlen_q, D
   auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
   const size_t rows = static_cast<size_t>(s->total_q) * s->num_heads_q;
   L->qp = take(rows * s->head_dim * 2);
-  L->op = take(rows * s->head_dim * 2);
-  L->lsep = take(rows * 4);
   L->qr2 = take(static_cast<size_t>(R2) * 8);
   L->kr2 = take(static_cast<size_t>(R2) * 8);
   L->ty2 = take(static_cast<size_t>(R2) * 4);
@@ -211,19 +188,20 @@ int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const v
   c.q = wb + L.qp; c.k = k; c.v = v;
   c.q_ranges = qr2; c.k_ranges = kr2; c.types = ty2; c.n_ranges = static_cast<int32_t>(L.R2);
   c.softmax_scale = softmax_scale; c.softcap = softcap;
-  c.out = wb + L.op; c.lse = reinterpret_cast<float*>(wb + L.lsep);
+  // (the packed problem's O and LSE have the caller's sizes; with the key split nothing but
+  // the merge writes them, through the unpacking map below)
+  c.out = out; c.lse = lse;
   c.status = status; c.stream = stream; c.options = options;
   c.alibi_pack = P;
   c.key_split = true;
+  // every packed row goes through the LSE merge, which writes the caller's layout directly
+  c.unpack_out = out;
+  c.unpack_lse = lse;
   if (page_table != nullptr) {
     c.paged = true;
     c.page_table = page_table; c.page_size = page_size; c.n_pages = n_pages;
   }
-  const int rc = fwd_with_workspace(c, wb + L.inner, workspace_bytes - L.inner);
-  if (rc != FFA_OK) return rc;
-  decode_unpack<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(wb + L.op), static_cast<uint4*>(out),
-                                       reinterpret_cast<const float*>(wb + L.lsep), lse, nq, hq, P, d);
-  return cudaGetLastError() == cudaSuccess ? FFA_OK : FFA_ERR_CUDA;
+  return fwd_with_workspace(c, wb + L.inner, workspace_bytes - L.inner);
 }
 
 }  // extern "C"

@@ -111,6 +111,12 @@ struct FwdParams {
   // member: placed earlier, it changed the register allocation of the other kernels.)
   int key_split;
   float cap_q5[3];  // cap_q in degree 5 (kTanhPoly5): the bounded-softcap kernel's form
+  // Decoding (key split): the merge writes O and LSE straight into the caller's token-major
+  // layout, row r of packed head h being token r / upack of query head h * upack + r % upack
+  // (out [nq / upack, hq * upack, D], lse [hq * upack, nq / upack]); null: packed layout
+  __nv_bfloat16* uout;
+  float* ulse;
+  int upack;
 };
 
 struct Item {
@@ -1049,11 +1055,18 @@ __global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParam
 #pragma unroll
   for (int w = 1; w < kMergeWarps; ++w) mx = fmaxf(mx, sh_max[w]);
   __nv_bfloat16* out = p.out + (static_cast<size_t>(row) * p.hq + h) * D;
+  float* lse_at = p.lse + static_cast<size_t>(h) * p.nq + row;
+  if (p.uout != nullptr) {
+    const int tok = row / p.upack, hu = h * p.upack + row % p.upack;
+    const int ntok = p.nq / p.upack;
+    out = p.uout + (static_cast<size_t>(tok) * p.hq * p.upack + hu) * D;
+    lse_at = p.ulse + static_cast<size_t>(hu) * ntok + tok;
+  }
   if (mx == -INFINITY) {
     if (warp == 0) {
 #pragma unroll
       for (int k = 0; k < kPer; ++k) out[lane * kPer + k] = __float2bfloat16(0.0f);
-      if (lane == 0) p.lse[static_cast<size_t>(h) * p.nq + row] = -INFINITY;
+      if (lane == 0) *lse_at = -INFINITY;
     }
     return;
   }
@@ -1098,7 +1111,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParam
       }
       *reinterpret_cast<uint32_t*>(out + lane * kPer + k) = pack_bf16x2(a0 * inv, a1 * inv);
     }
-    if (lane == 0) p.lse[static_cast<size_t>(h) * p.nq + row] = mx + lg2_approx(tw) * kLn2;
+    if (lane == 0) *lse_at = mx + lg2_approx(tw) * kLn2;
   }
 }
 
@@ -1147,6 +1160,9 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   p.plan = a.plan;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
+  p.uout = static_cast<__nv_bfloat16*>(a.unpack_out);
+  p.ulse = a.unpack_lse;
+  p.upack = a.unpack_out != nullptr ? a.alibi_pack : 1;
   p.alibi = a.alibi;
   p.alibi_pack = a.alibi_pack;
   p.page_table = a.page_table;

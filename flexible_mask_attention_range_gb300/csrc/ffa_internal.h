@@ -238,6 +238,10 @@ struct FwdArgs {
   int head_pair, ngrp, slots, n_items;  // n_items: upper bound (chunks x slots) for the grid
   int split;
   int key_split = 0;  // WsLayout::key_split
+  // key split only: the LSE merge writes O [nq / alibi_pack, hq * alibi_pack, d] and LSE
+  // [hq * alibi_pack, nq / alibi_pack] here (the caller's token-major layout), not out / lse
+  void* unpack_out = nullptr;
+  float* unpack_lse = nullptr;
   float scale, softcap;
   const void *q, *k, *v;
   void* out;
@@ -299,6 +303,8 @@ struct FwdCall {
   int64_t n_pages = 0;
   int alibi_pack = 0;  // > 0: rows are packed (token, query head) pairs (decode), see FwdArgs
   bool key_split = false;  // WsLayout::key_split (decode)
+  void* unpack_out = nullptr;  // FwdArgs::unpack_out
+  float* unpack_lse = nullptr;
 };
 // Shape check shared by the entry points (FFA_OK or the error code).
 int check_shape(const ffa_shape* s, int32_t n_ranges);
