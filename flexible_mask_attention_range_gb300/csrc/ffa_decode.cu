@@ -21,7 +21,7 @@
 // slices, one per token i, over the keys that token sees under the bottom-right alignment
 // used everywhere in this library (j <= i + ke - qe).  max_seqlen_q bounds m, so the
 // rewritten list has a fixed length n_ranges * max_seqlen_q (unused entries are empty
-// slices).  Packing and rewriting are two small kernels before the forward pass (dense or
+// slices).  Packing and rewriting share one small kernel before the forward pass (dense or
 // paged); the forward pass's LSE merge writes O and LSE in the caller's layout.  With ALiBi (FlexAttention paper, sections 2 and 3.1; decoding with GQA
 // and ALiBi is one of the cases its section 6 measures) a packed row keeps the slope of its
 // query head and the position of its token, so the bias is the one of the unpacked problem.
@@ -33,14 +33,15 @@
 namespace ffa {
 namespace {
 
-// q [N, Hq, d] -> qp [N * P, Hq / P, d], in 16-byte units (d / 8 of them per row).
-__global__ void __launch_bounds__(256) decode_pack_q(const uint4* __restrict__ q, uint4* __restrict__ qp,
-                                                     int64_t n, int hq, int P, int d) {
+// q [N, Hq, d] -> qp [N * P, Hq / P, d], in 16-byte units (d / 8 of them per row); block b of
+// nb blocks.
+__device__ void decode_pack_q(const uint4* __restrict__ q, uint4* __restrict__ qp, int64_t n, int hq, int P, int d,
+                              int b, int nb) {
   const int hp = hq / P;
   const int64_t per_row = d / 8;
   const int64_t total = n * hq * per_row;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  for (int64_t idx = b * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(nb) * blockDim.x) {
     const int64_t row = idx / per_row, c = idx - row * per_row;  // packed row = (i * P + g) * hp + h
     const int64_t h = row % hp, ig = row / hp;
     const int64_t g = ig % P, i = ig / P;
@@ -50,14 +51,14 @@ __global__ void __launch_bounds__(256) decode_pack_q(const uint4* __restrict__ q
 
 // Slice s, token slot u -> rewritten slice s * M + u (see the file comment).  Invalid slices
 // (bounds, type, or a CAUSAL slice longer than M) are reported with FFA_STATUS_BAD_RANGE and
-// dropped, as the planner does for the plain forward pass.
-__global__ void __launch_bounds__(256) decode_slices(const int32_t* __restrict__ qr, const int32_t* __restrict__ kr,
-                                                     const int32_t* __restrict__ ty, int R, int M, int P, int64_t nq,
-                                                     int64_t nk, int32_t* __restrict__ qr2, int32_t* __restrict__ kr2,
-                                                     int32_t* __restrict__ ty2, int32_t* status) {
+// dropped, as the planner does for the plain forward pass.  Block b of nb blocks.
+__device__ void decode_slices(const int32_t* __restrict__ qr, const int32_t* __restrict__ kr,
+                              const int32_t* __restrict__ ty, int R, int M, int P, int64_t nq, int64_t nk,
+                              int32_t* __restrict__ qr2, int32_t* __restrict__ kr2, int32_t* __restrict__ ty2,
+                              int32_t* status, int b, int nb) {
   const int64_t total = static_cast<int64_t>(R) * M;
-  for (int64_t slot = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; slot < total;
-       slot += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  for (int64_t slot = b * static_cast<int64_t>(blockDim.x) + threadIdx.x; slot < total;
+       slot += static_cast<int64_t>(nb) * blockDim.x) {
     const int64_t s = slot / M;
     const int u = static_cast<int>(slot - s * M);
     const int64_t qs = qr[2 * s], qe = qr[2 * s + 1], ks = kr[2 * s], ke = kr[2 * s + 1];
@@ -84,6 +85,21 @@ __global__ void __launch_bounds__(256) decode_slices(const int32_t* __restrict__
     kr2[2 * slot + 1] = static_cast<int32_t>(e);
     ty2[slot] = FFA_FULL;
   }
+}
+
+// Both preparation steps in one launch: the first pack_blocks blocks pack q, the others
+// rewrite the slices.
+__global__ void __launch_bounds__(256) decode_prepare(const uint4* __restrict__ q, uint4* __restrict__ qp, int64_t n,
+                                                      int hq, int P, int d, int pack_blocks,
+                                                      const int32_t* __restrict__ qr, const int32_t* __restrict__ kr,
+                                                      const int32_t* __restrict__ ty, int R, int M, int64_t nk,
+                                                      int32_t* __restrict__ qr2, int32_t* __restrict__ kr2,
+                                                      int32_t* __restrict__ ty2, int32_t* status) {
+  if (static_cast<int>(blockIdx.x) < pack_blocks)
+    decode_pack_q(q, qp, n, hq, P, d, blockIdx.x, pack_blocks);
+  else
+    decode_slices(qr, kr, ty, R, M, P, n, nk, qr2, kr2, ty2, status, blockIdx.x - pack_blocks,
+                  gridDim.x - pack_blocks);
 }
 
 // Query heads per packed row group: all G of a key/value head.
@@ -170,17 +186,15 @@ int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const v
   const int nsm = num_sms();
   const int64_t units = nq * hq * (d / 8);
   const int blocks = static_cast<int>(units / 256 + 1 < static_cast<int64_t>(nsm) * 8 ? units / 256 + 1 : nsm * 8);
-  decode_pack_q<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(q), reinterpret_cast<uint4*>(wb + L.qp), nq, hq, P, d);
-  if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   int32_t* qr2 = reinterpret_cast<int32_t*>(wb + L.qr2);
   int32_t* kr2 = reinterpret_cast<int32_t*>(wb + L.kr2);
   int32_t* ty2 = reinterpret_cast<int32_t*>(wb + L.ty2);
-  if (L.R2 > 0) {
-    const int sb = static_cast<int>(L.R2 / 256 + 1 < static_cast<int64_t>(nsm) * 4 ? L.R2 / 256 + 1 : nsm * 4);
-    decode_slices<<<sb, 256, 0, s>>>(q_ranges, k_ranges, attn_type_map, n_ranges, max_seqlen_q, P, nq,
-                                     shape->total_k, qr2, kr2, ty2, status);
-    if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
-  }
+  const int sb = L.R2 > 0 ? static_cast<int>(L.R2 / 256 + 1 < static_cast<int64_t>(nsm) * 4 ? L.R2 / 256 + 1 : nsm * 4)
+                          : 0;
+  decode_prepare<<<blocks + sb, 256, 0, s>>>(static_cast<const uint4*>(q), reinterpret_cast<uint4*>(wb + L.qp), nq, hq,
+                                             P, d, blocks, q_ranges, k_ranges, attn_type_map, n_ranges, max_seqlen_q,
+                                             shape->total_k, qr2, kr2, ty2, status);
+  if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   // the forward pass over the packed problem; with ALiBi each packed row takes the slope of
   // its query head and the position of its token (FwdArgs::alibi_pack)
   FwdCall c;

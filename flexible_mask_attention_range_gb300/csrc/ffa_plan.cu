@@ -365,6 +365,11 @@ __global__ void __launch_bounds__(1024) plan_chunks_kernel(int ngrp, int split_l
   }
   if (threadIdx.x == 0) v.hdr[1] = base;
   __syncthreads();
+  if (all_split) {  // key split: the chunks are all split_len long but each group's last, so
+                    // their own order is already (nearly) longest first
+    for (int i = threadIdx.x; i < base; i += blockDim.x) v.chunk_order[i] = i;
+    return;
+  }
   counting_sort_desc(v.chunk_len, base, split_len, v.chunk_order, hist, warp_buf);
 }
 
