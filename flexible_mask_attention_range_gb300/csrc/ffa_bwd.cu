@@ -14,7 +14,8 @@
 //      tcgen05 GEMMs per step: S^T = K Q^T and dP^T = V dO^T (keys on TMEM lanes), then
 //      dV += P^T dO and dK += dS^T Q with P^T / dS^T read from TMEM, and dQ = dS K with dS
 //      staged in shared memory; dQ is added into the fp32 accumulator with TMA bulk
-//      reduce-adds (cp.reduce.async.bulk.tensor, add) of 32-column boxes.
+//      reduce-adds (cp.reduce.async.bulk.tensor, add) of 32-column boxes staged in a buffer
+//      of their own, so the next step's dS^T may be written as soon as the dQ MMA has run.
 //      dK and dV stay in TMEM for the whole item and are written once.
 //   3. ffa_bwd_dq_convert: fp32 accumulator -> bf16 dq.
 //
@@ -45,20 +46,25 @@ constexpr int kWarpMma = 13;
 
 template <int D>
 struct BwdSmem {
-  static constexpr int kStages = D == 128 ? 2 : 3;
+  // Q (with its row statistics) and dO rings; at d = 128 dO has one slot, so that the dQ drain
+  // has a staging buffer of its own
+  static constexpr int kStagesQ = D == 128 ? 2 : 3;
+  static constexpr int kStagesDO = D == 128 ? 1 : 3;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kBoxBytes = kTile * 128;
   static constexpr int kStatBytes = 2 * kTile * 4;  // LSE*log2e and D of one query tile
   static constexpr int kK = 0;
   static constexpr int kV = kTileBytes;
   static constexpr int kQ = 2 * kTileBytes;                        // + s * kTileBytes
-  static constexpr int kDO = kQ + kStages * kTileBytes;            // + s * kTileBytes
-  static constexpr int kDS = kDO + kStages * kTileBytes;           // 128 keys x 128 queries bf16
-  static constexpr int kStat = kDS + kTile * kTile * 2;            // + s * kStatBytes
-  static constexpr int kBar = kStat + kStages * kStatBytes;
-  // kv_full, kv_empty, qdo_full[S], qdo_empty[S], s_full, dp_full, p_full, ds_full, dq_full,
-  // dq_empty, dkv_full, drain, sds_free, stall (never arrived on; failure-detection test)
-  static constexpr int kNumBars = 2 + 2 * kStages + 10;
+  static constexpr int kDO = kQ + kStagesQ * kTileBytes;           // + s * kTileBytes
+  static constexpr int kDS = kDO + kStagesDO * kTileBytes;         // 128 keys x 128 queries bf16
+  static constexpr int kDQS = kDS + kTile * kTile * 2;             // dQ staging: two 128 x 32 fp32 boxes
+  static constexpr int kStat = kDQS + 2 * kTile * 128;             // + s * kStatBytes
+  static constexpr int kBar = kStat + kStagesQ * kStatBytes;
+  // kv_full, kv_empty, q_full[SQ], q_empty[SQ], do_full[SD], do_empty[SD], s_full, dp_full,
+  // p_full, ds_full, dq_full, dq_empty, dkv_full, drain, stall (never arrived on;
+  // failure-detection test)
+  static constexpr int kNumBars = 2 + 2 * kStagesQ + 2 * kStagesDO + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kMaxDyn = 232448;
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using SM = BwdSmem<D>;
-  constexpr int S = SM::kStages;
+  constexpr int SQ = SM::kStagesQ, SD = SM::kStagesDO;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad + SM::kTotal > SM::kAlloc) {  // cannot place the swizzled tiles: report and stop
@@ -264,18 +270,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::kBar);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
-  uint64_t* qdo_full = bars + 2;
-  uint64_t* qdo_empty = bars + 2 + S;
-  uint64_t* s_full = bars + 2 + 2 * S;
+  uint64_t* q_full = bars + 2;
+  uint64_t* q_empty = q_full + SQ;
+  uint64_t* do_full = q_empty + SQ;
+  uint64_t* do_empty = do_full + SD;
+  uint64_t* s_full = do_empty + SD;
   uint64_t* dp_full = s_full + 1;
   uint64_t* p_full = s_full + 2;
   uint64_t* ds_full = s_full + 3;
-  uint64_t* dq_full = s_full + 4;
+  uint64_t* dq_full = s_full + 4;  // the dQ MMA has run: dQ in TMEM, the dS^T tile free again
   uint64_t* dq_empty = s_full + 5;
   uint64_t* dkv_full = s_full + 6;
   uint64_t* drain = s_full + 7;
-  uint64_t* sds_free = s_full + 8;
-  uint64_t* stall_bar = s_full + 9;
+  uint64_t* stall_bar = s_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM::kMisc + 4);
 
@@ -283,9 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&qdo_full[s], 1);
-      mbar_init(&qdo_empty[s], 1);
+    for (int s = 0; s < SQ; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < SD; ++s) {
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -295,7 +306,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_empty, 128);
     mbar_init(dkv_full, 1);
     mbar_init(drain, 1);
-    mbar_init(sds_free, 1);
     mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -349,11 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t e = it.ent(t / p.G);
         const int qt = entry_idx(e);
         const int cls = entry_cls(e, 0);
-        const uint32_t st = step_cnt % S;
+        const uint32_t st = step_cnt % SQ;
         const float* stat = reinterpret_cast<const float*>(sm + SM::kStat + st * SM::kStatBytes);
-        // the row statistics arrive with the stage's Q/dO (qdo_full); S^T with s_full
+        // the row statistics arrive with the step's Q (q_full); S^T with s_full
         uint64_t* sb = (p.stall && step_cnt == 0) ? stall_bar : s_full;
-        ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (step_cnt / S) & 1u, abort_flag, lim) &&
+        ok = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (step_cnt / SQ) & 1u, abort_flag, lim) &&
                                          mbar_wait(sb, step_cnt & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
@@ -489,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(p_full);
         // phase 2: dS^T = P' (dP^T - D) -> TMEM (for dK) and shared memory (for dQ)
         ok = __all_sync(0xffffffffu, mbar_wait(dp_full, step_cnt & 1u, abort_flag, lim));
-        if (ok && step_cnt > 0)  // the previous step's dQ no longer uses sDS (MMA operand, then staging)
-          ok = __all_sync(0xffffffffu, mbar_wait(sds_free, (step_cnt - 1) & 1u, abort_flag, lim));
+        if (ok && step_cnt > 0)  // the previous step's dQ MMA (the dS^T tile's reader) has run
+          ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (step_cnt - 1) & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
         const float* Drow = stat + kTile;
@@ -563,13 +573,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ dQ warpgroup
     // Reads its dQ row from TMEM (64 columns at a time; the columns are released once the
     // whole row is in registers), then adds the tile into the fp32 accumulator with TMA bulk
-    // reduce-adds of 32-column boxes staged through the two 16 KB halves of the dS^T shared
-    // tile (free once the dQ MMA has consumed it).
+    // reduce-adds of 32-column boxes staged through the two 16 KB halves of its own staging
+    // buffer, box after box; a half is rewritten once the reduce issued from it two boxes
+    // before has read it, so the drain of one step runs on while the next step computes.
     const int q4 = warp - kWarpDq;
     const int r = q4 * 32 + lane;
     const bool leader = (q4 == 0 && lane == 0);
     const uint32_t tQ = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + 128;
-    uint8_t* sDS = sm + SM::kDS;
+    uint8_t* sDQS = sm + SM::kDQS;  // two 16 KB halves, used alternately box after box
     uint32_t step_cnt = 0;
     bool ok = true;
     for (int wave = 0; ok; ++wave) {
@@ -599,11 +610,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int c = 2 * half + cc;
-            uint8_t* buf = sDS + (c & 1) * (kTile * 128);
-            if (c >= 2) {  // the reduce issued from this half two chunks ago has read it
-              if (leader) bulk_wait_group_read<1>();
-              named_bar_sync(1, 128);
-            }
+            uint8_t* buf = sDQS + (c & 1) * (kTile * 128);
+            // the reduce issued from this half two boxes ago (in this step or the previous
+            // one) has read it
+            if (leader) bulk_wait_group_read<1>();
+            named_bar_sync(1, 128);
             uint8_t* rowp = buf + r * 128;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -628,15 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (leader) {
-          if (kDet) {  // the additions must have landed before the next key tile may add
-            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-            fence_proxy_async_global();
-            if (turn) red_release_gpu_add(p.dq_sem + static_cast<size_t>(h) * p.nqt + qt, 1);
-          } else {
-            bulk_wait_group_read<0>();
-          }
-          mbar_arrive(sds_free);
+        if (kDet && leader) {  // the additions must have landed before the next key tile may add
+          asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+          fence_proxy_async_global();
+          if (turn) red_release_gpu_add(p.dq_sem + static_cast<size_t>(h) * p.nqt + qt, 1);
         }
         ++step_cnt;
       }
@@ -648,8 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t item_cnt = 0, gq = 0;
       bool ok = true;
-      int last_use[S];
-      for (int s = 0; s < S; ++s) last_use[s] = -1;
+      int last_q[SQ], last_do[SD];  // the last use of each slot whose copies were issued
+      for (int s = 0; s < SQ; ++s) last_q[s] = -1;
+      for (int s = 0; s < SD; ++s) last_do[s] = -1;
       int last_kv = -1;
       for (int wave = 0; ok; ++wave) {
         const int item = sched_item(wave);
@@ -670,24 +677,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < it.n_steps; ++t) {
           const int qt = entry_idx(it.ent(t / p.G));
           const int h = it.kvh * p.G + (t % p.G);
-          const uint32_t st = gq % S, u = gq / S;
+          // Q and its row statistics (released after the step's dK MMA), then dO (released
+          // after the step's dV MMA)
+          const uint32_t st = gq % SQ, u = gq / SQ;
           if (u > 0) {
-            ok = mbar_wait(&qdo_empty[st], (u - 1) & 1u, abort_flag, lim);
+            ok = mbar_wait(&q_empty[st], (u - 1) & 1u, abort_flag, lim);
             if (!ok) break;
           }
-          mbar_arrive_expect_tx(&qdo_full[st], 2 * SM::kTileBytes + SM::kStatBytes);
+          mbar_arrive_expect_tx(&q_full[st], SM::kTileBytes + SM::kStatBytes);
 #pragma unroll
-          for (int b = 0; b < D / 64; ++b) {
-            tma_load_2d(sm + SM::kQ + st * SM::kTileBytes + b * SM::kBoxBytes, &tmQ, &qdo_full[st],
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_2d(sm + SM::kQ + st * SM::kTileBytes + b * SM::kBoxBytes, &tmQ, &q_full[st],
                         h * D + 64 * b, qt * kTile);
-            tma_load_2d(sm + SM::kDO + st * SM::kTileBytes + b * SM::kBoxBytes, &tmDO, &qdo_full[st],
-                        h * D + 64 * b, qt * kTile);
-          }
           const size_t so = static_cast<size_t>(h) * p.qpad + static_cast<size_t>(qt) * kTile;
           uint8_t* sst = sm + SM::kStat + st * SM::kStatBytes;
-          bulk_load(sst, p.lse2 + so, kTile * 4, &qdo_full[st]);
-          bulk_load(sst + kTile * 4, p.rowD + so, kTile * 4, &qdo_full[st]);
-          last_use[st] = static_cast<int>(u);
+          bulk_load(sst, p.lse2 + so, kTile * 4, &q_full[st]);
+          bulk_load(sst + kTile * 4, p.rowD + so, kTile * 4, &q_full[st]);
+          last_q[st] = static_cast<int>(u);
+          const uint32_t sd = gq % SD, ud = gq / SD;
+          if (ud > 0) {
+            ok = mbar_wait(&do_empty[sd], (ud - 1) & 1u, abort_flag, lim);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(&do_full[sd], SM::kTileBytes);
+#pragma unroll
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_2d(sm + SM::kDO + sd * SM::kTileBytes + b * SM::kBoxBytes, &tmDO, &do_full[sd],
+                        h * D + 64 * b, qt * kTile);
+          last_do[sd] = static_cast<int>(ud);
           ++gq;
         }
         ++item_cnt;
@@ -696,8 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_abort(abort_flag, p.status);
         const uint64_t short_lim = 100000000ull;
         if (last_kv >= 0) mbar_wait(kv_full, static_cast<uint32_t>(last_kv) & 1u, nullptr, short_lim);
-        for (int s = 0; s < S; ++s)
-          if (last_use[s] >= 0) mbar_wait(&qdo_full[s], static_cast<uint32_t>(last_use[s]) & 1u, nullptr, short_lim);
+        for (int s = 0; s < SQ; ++s)
+          if (last_q[s] >= 0) mbar_wait(&q_full[s], static_cast<uint32_t>(last_q[s]) & 1u, nullptr, short_lim);
+        for (int s = 0; s < SD; ++s)
+          if (last_do[s] >= 0) mbar_wait(&do_full[s], static_cast<uint32_t>(last_do[s]) & 1u, nullptr, short_lim);
       }
     }
     __syncwarp();
@@ -720,32 +739,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(kv_full, item_cnt & 1u, abort_flag, lim);
         if (!ok) break;
         {  // S^T of the item's first step
-          const uint32_t st = gq % S;
-          ok = mbar_wait(&qdo_full[st], (gq / S) & 1u, abort_flag, lim);
+          const uint32_t st = gq % SQ;
+          ok = mbar_wait(&q_full[st], (gq / SQ) & 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
           issue_kmajor<D>(tS, sK, sQ + st * SM::kTileBytes, idesc_st);  // S^T = K Q^T
           umma_commit(s_full);
         }
         for (int t = 0; t < it.n_steps; ++t) {
-          const uint32_t st = gq % S;
-          const uint32_t q_s = sQ + st * SM::kTileBytes, do_s = sDO + st * SM::kTileBytes;
+          const uint32_t st = gq % SQ, sd = gq % SD;
+          const uint32_t q_s = sQ + st * SM::kTileBytes, do_s = sDO + sd * SM::kTileBytes;
           if (gq > 0) {  // the previous dQ has been drained from the dP^T columns
             ok = mbar_wait(dq_empty, (gq - 1) & 1u, abort_flag, lim);
             if (!ok) break;
-            tc_fence_after();
           }
+          ok = mbar_wait(&do_full[sd], (gq / SD) & 1u, abort_flag, lim);
+          if (!ok) break;
+          tc_fence_after();
           issue_kmajor<D>(tP, sV, do_s, idesc_st);  // dP^T = V dO^T
           umma_commit(dp_full);
           ok = mbar_wait(p_full, gq & 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
           issue_ts<D>(tDV, tS, do_s, idesc_acc, t > 0);  // dV += P^T dO
+          umma_commit(&do_empty[sd]);                     // dO's last reader
           if (t + 1 < it.n_steps) {
             // S^T of the next step now, so P^T of step t+1 is computed while dK and dQ of this
             // step run (P^T of step t has been read by the dV MMA issued just before)
-            const uint32_t g1 = gq + 1, st1 = g1 % S;
-            ok = mbar_wait(&qdo_full[st1], (g1 / S) & 1u, abort_flag, lim);
+            const uint32_t g1 = gq + 1, st1 = g1 % SQ;
+            ok = mbar_wait(&q_full[st1], (g1 / SQ) & 1u, abort_flag, lim);
             if (!ok) break;
             tc_fence_after();
             issue_kmajor<D>(tS, sK, sQ + st1 * SM::kTileBytes, idesc_st);
@@ -757,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_ts<D>(tDK, tP, q_s, idesc_acc, t > 0);  // dK += dS^T Q
           issue_dq<D>(tP, sDS, sK, idesc_dq);           // dQ = dS K (into the dP^T columns)
           umma_commit(dq_full);
-          umma_commit(&qdo_empty[st]);
+          umma_commit(&q_empty[st]);
           ++gq;
         }
         if (!ok) break;
