@@ -375,9 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // phase 1: P^T of this warpgroup's 64 queries from S^T and the row LSEs; keep
         // P' = P (or P (1 - tanh^2) with softcap) packed as bf16 for phase 2
         uint32_t pp[32];
-        // kM: this tile may hide elements (mk says whether it does).  Without softcap the loop
-        // exists twice so fully visible tiles carry no per-element mask test; with softcap one
-        // copy is kept (a second one costs registers there).
+        // kM: this tile may hide elements (mk says whether it does).  The loop exists twice so
+        // fully visible tiles carry no per-element mask test.
         auto p1_body = [&](auto mtag, bool mk) {
         constexpr bool kM = decltype(mtag)::value;
 #pragma unroll
@@ -487,10 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(tS + 16 * c, pk);
         }
         };
-        if (kCap) {
+        // One copy per warp: the tensor-memory loads and stores and the polynomial's vote in the
+        // pass are warp-collective, so the warp takes the masking copy when any of its key rows
+        // needs a mask (a ragged last key tile masks some lanes only), each lane with its own mk.
+        if (__any_sync(0xffffffffu, masked)) {
           p1_body(std::true_type{}, masked);
-        } else if (masked) {
-          p1_body(std::true_type{}, true);
         } else {
           p1_body(std::false_type{}, false);
         }
