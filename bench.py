@@ -540,10 +540,10 @@ def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
 # source changes the figure no longer describes the kernel, and `traffic` is reported null.
 TRAFFIC = {
     # (workload, kernel): (bytes per launch, source hash at capture)
-    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1865140736 + 238864640, "8e8b1e55a6b6f635"),
-    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (13556390400 + 6666823680, "e5815c4bacf7da2d"),
-    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541301504 + 239793920, "8e8b1e55a6b6f635"),
-    ("sliding_32k_softcap", "ffa_bwd_kernel"): (2690292480 + 1356663040, "e5815c4bacf7da2d"),
+    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1858416896 + 238822912, "8e8b1e55a6b6f635"),
+    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (29713646080 + 15384594944, "8185946a66dd5dfa"),
+    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541342976 + 239251456, "8e8b1e55a6b6f635"),
+    ("sliding_32k_softcap", "ffa_bwd_kernel"): (2698729472 + 1364480256, "8185946a66dd5dfa"),
 }
 
 
