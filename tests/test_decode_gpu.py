@@ -178,3 +178,37 @@ def test_decode_alibi(n_seq, q_len, hq, hkv, d, cap, paged, seed):
     # the token-major forward pass with the same slopes agrees up to summation order
     assert (o.float() - o_f.float()).abs().max().item() <= 2e-2
     assert (l - l_f).abs().max().item() <= 1e-3
+
+
+@pytest.mark.parametrize("kv_len,hq,hkv,cap", [(100, 8, 2, 0.0), (128, 16, 2, 30.0), (129, 12, 4, 0.0)])
+def test_decode_one_or_two_key_tiles(kv_len, hq, hkv, cap):
+    # one sequence with a cache of one key tile (the key split's second warpgroup has no tile
+    # and leaves an empty partial) or just over one tile (one tile each)
+    qr, kr, ty = [[0, 1]], [[0, kv_len]], [O.CAUSAL]
+    g = W.make_generator(300 + kv_len)
+    d = 128
+    q = torch.randn(1, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(kv_len, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(kv_len, hkv, d, generator=g).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, l = ffa.ffa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), qr, kr, ty, max_seqlen_q=1, softcap=cap,
+                              status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ro, rl = O.forward(q, k, v, qr, kr, ty, softcap=cap)
+    assert_out_close(to64(o), ro)
+    assert_lse_close(to64(l), rl)
+
+
+def test_decode_without_keys():
+    # an empty cache: every row is empty, O = 0 and LSE = -inf in the caller's layout
+    hq, hkv, d = 8, 2, 64
+    q = torch.randn(3, hq, d).to(torch.bfloat16).cuda()
+    k = torch.zeros(0, hkv, d, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(0, hkv, d, dtype=torch.bfloat16, device="cuda")
+    qr, kr, ty = [[0, 3]], [[0, 0]], [O.FULL]
+    out = torch.full((3, hq, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(hq, 3, dtype=torch.float32, device="cuda")
+    o, l = ffa.ffa_fwd_decode(q, k, v, qr, kr, ty, max_seqlen_q=3, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(o).item() == 0 and bool(torch.isinf(l).all()) and bool((l < 0).all())
