@@ -540,10 +540,10 @@ def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
 # source changes the figure no longer describes the kernel, and `traffic` is reported null.
 TRAFFIC = {
     # (workload, kernel): (bytes per launch, source hash at capture)
-    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1858416896 + 238822912, "8e8b1e55a6b6f635"),
-    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (29713646080 + 15384594944, "8185946a66dd5dfa"),
-    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541342976 + 239251456, "8e8b1e55a6b6f635"),
-    ("sliding_32k_softcap", "ffa_bwd_kernel"): (2698729472 + 1364480256, "8185946a66dd5dfa"),
+    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1852932096 + 238630912, "8e8b1e55a6b6f635"),
+    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (22227209984 + 11355497472, "c5d2c680902023ff"),
+    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541329408 + 239036672, "8e8b1e55a6b6f635"),
+    ("sliding_32k_softcap", "ffa_bwd_kernel"): (2689280000 + 1354965248, "c5d2c680902023ff"),
 }
 
 
