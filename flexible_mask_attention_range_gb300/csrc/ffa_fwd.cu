@@ -56,6 +56,25 @@ static_assert(2 * kRegsSoftmax + kRegsProducer == 3 * kRegsLaunch, "per sub-part
 static_assert(kThreads * kRegsLaunch <= 65536, "launch register file");
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpDec = 10;  // item decoder: stages the next work items for the softmax warps
+constexpr int kStageSl = 4;   // slices of a query tile staged with its item
+
+// One work item as the softmax warpgroups need it, staged in shared memory by the decoder warp
+// ahead of use: the item's chunk, the first list entry of each warpgroup, and per warpgroup
+// the slices touching its query tile (when at most kStageSl do; else the warpgroup reads the
+// planner's list from global memory).  A slot is released when the item's epilogue is done.
+struct ItemStage {
+  int4 ch;  // the item's chunk (group, first entry, end entry, partial slot)
+  uint32_t e_first[2];
+  int pad0[2];
+  struct Tile {
+    int nsl;  // row_nsl of the query tile (0 past the last query tile)
+    int type[kStageSl];
+    int pad[3];
+    int4 s[kStageSl];
+  } tile[2];
+};
+static_assert(sizeof(ItemStage) <= 256, "item staging slot");
 
 template <int D>
 struct FwdSmem {
@@ -69,12 +88,15 @@ struct FwdSmem {
   // output staging: one 128-row x 64-column bf16 box per softmax warpgroup
   static constexpr int kOst = kV + kStages * kTileBytes;
   static constexpr int kOstBytes = kTile * 128;
-  static constexpr int kBar = kOst + 2 * kOstBytes;
+  // two work-item staging slots (ItemStage)
+  static constexpr int kIt = kOst + 2 * kOstBytes;
+  static constexpr int kItBytes = 256;
+  static constexpr int kBar = kIt + 2 * kItBytes;
   // q_full, q_empty, k_full[S+1], v_full[S+1], kv_empty[S+1], s_full[2], p_full[2], o_full[2],
-  // drain, stall (never arrived on; the failure-detection test waits on it).  Slot S exists
-  // with the key split only: its K sits in the (then unused) second query tile, its V in the
-  // (then unused) output staging boxes.
-  static constexpr int kNumBars = 2 + 3 * (kStages + 1) + 8;
+  // drain, stall (never arrived on; the failure-detection test waits on it), it_full[2],
+  // it_empty[2].  Slot S exists with the key split only: its K sits in the (then unused)
+  // second query tile, its V in the (then unused) output staging boxes.
+  static constexpr int kNumBars = 2 + 3 * (kStages + 1) + 12;
   static_assert(kTileBytes <= 2 * kTile * 128, "a V tile fits the two output staging boxes");
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
@@ -127,11 +149,13 @@ struct Item {
 };
 
 // Work item -> (chunk of a group's work list, head slot).  Chunks are taken longest first.
+__device__ __forceinline__ int4 item_chunk(const FwdParams& p, int item) {
+  return p.plan.chunks[p.plan.chunk_order[item / p.slots]];
+}
 template <bool kKS>
-__device__ __forceinline__ Item decode_item(const FwdParams& p, int item) {
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int item, int4 ch) {
   Item it;
-  const int rank = item / p.slots, slot = item - rank * p.slots;
-  const int4 ch = p.plan.chunks[p.plan.chunk_order[rank]];
+  const int slot = item - (item / p.slots) * p.slots;
   it.g = ch.x;
   it.n = ch.z - ch.y;
   it.pslot = ch.w;
@@ -151,6 +175,10 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int item) {
   }
   it.kvh = it.h0 / p.G;
   return it;
+}
+template <bool kKS>
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int item) {
+  return decode_item<kKS>(p, item, item_chunk(p, item));
 }
 
 // Static snake schedule over the longest-first item order.
@@ -204,7 +232,7 @@ __device__ __forceinline__ void row_mask(const FwdParams& p, int cls, int row, i
 
 // Element mask of query row `row` over key tile kt from the row's visible intervals (when the
 // union of its slices has at most two) or from the slice list.
-__device__ __forceinline__ void tile_mask(const FwdParams& p, int cls, int row, int kt, int nsl, const int* sl,
+__device__ __forceinline__ void tile_mask(const FwdParams& p, int cls, int row, int kt, const int* nsl_p, int qt,
                                           bool ivl_ok, int ilo0, int ihi0, int ilo1, int ihi1, uint32_t (&w)[4]) {
   if (ivl_ok && cls != FFA_TILE_FULL) {
     const int c0 = kt * kTile;
@@ -221,23 +249,27 @@ __device__ __forceinline__ void tile_mask(const FwdParams& p, int cls, int row, 
       for (int k = 0; k < 4; ++k) w[k] &= t4[k];
     }
   } else {
-    row_mask(p, cls, row, kt, nsl, sl, w);
+    // (the slice count is read here only: nsl_p points into the item's staging slot)
+    const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
+    row_mask(p, cls, row, kt, *nsl_p, sl, w);
   }
 }
 
 // The keys visible to query row `row` as at most two disjoint intervals (the union of the
-// row's slices, merged).  Returns false when the union needs more than two intervals.
-__device__ __forceinline__ bool row_intervals(const FwdParams& p, int row, int nsl, const int* sl, int& lo0,
-                                              int& hi0, int& lo1, int& hi1) {
+// n slices that fetch(k, slice, type) gives, merged).  Returns false when the union needs
+// more than two intervals.
+template <class F>
+__device__ __forceinline__ bool row_intervals_of(int row, int n, F&& fetch, int& lo0, int& hi0, int& lo1,
+                                                 int& hi1) {
   lo0 = hi0 = lo1 = hi1 = 0;
   int n_ivl = 0;
-  const int n = nsl >= 0 ? nsl : p.plan.hdr[0];
   for (int k = 0; k < n; ++k) {
-    const int si = nsl >= 0 ? sl[k] : k;
-    const int4 s = p.plan.slices[si];
+    int4 s;
+    int type;
+    fetch(k, s, type);
     if (row < s.x || row >= s.y) continue;
     const int lo = s.z;
-    const int hi = (p.plan.stypes[si] == FFA_CAUSAL) ? min(s.w, row + s.w - s.y + 1) : s.w;
+    const int hi = (type == FFA_CAUSAL) ? min(s.w, row + s.w - s.y + 1) : s.w;
     if (lo >= hi) continue;
     // merge with an existing interval when they overlap or touch
     if (n_ivl > 0 && lo <= hi0 && hi >= lo0) {
@@ -261,6 +293,20 @@ __device__ __forceinline__ bool row_intervals(const FwdParams& p, int row, int n
     }
   }
   return true;
+}
+
+// ... of the planner's slice list of the row's query tile (nsl < 0: every valid slice)
+__device__ __forceinline__ bool row_intervals(const FwdParams& p, int row, int nsl, const int* sl, int& lo0,
+                                              int& hi0, int& lo1, int& hi1) {
+  const int n = nsl >= 0 ? nsl : p.plan.hdr[0];
+  return row_intervals_of(
+      row, n,
+      [&](int k, int4& s, int& type) {
+        const int si = nsl >= 0 ? sl[k] : k;
+        s = p.plan.slices[si];
+        type = p.plan.stypes[si];
+      },
+      lo0, hi0, lo1, hi1);
 }
 
 // tanh(y) * C in the log2 domain from one exp2 and one reciprocal:
@@ -315,6 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_full = s_full + 4;
   uint64_t* drain = s_full + 6;
   uint64_t* stall_bar = s_full + 7;
+  uint64_t* it_full = s_full + 8;
+  uint64_t* it_empty = s_full + 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM::kMisc + 4);
 
@@ -334,6 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     mbar_init(stall_bar, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&it_full[t], 32);    // every lane of the decoder warp
+      mbar_init(&it_empty[t], 256);  // every softmax thread
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -377,12 +429,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int wave = 0; ok; ++wave) {
       const int item = sched_item(wave);
       if (item >= n_items) break;
-      const Item it = decode_item<kKS>(p, item);
+      // the item and its first entries from the decoder's slot; this row's visible keys from
+      // the slices staged there
+      const int ib = wave & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&it_full[ib], (wave >> 1) & 1u, abort_flag, lim));
+      if (!ok) break;
+      const ItemStage* ist = reinterpret_cast<const ItemStage*>(sm + SM::kIt) + ib;
+      const Item it = decode_item<kKS>(p, item, ist->ch);
       const int n = it.n;
       const int qt = wg ? it.qt1 : it.qt0;
       const int h = wg ? it.h1 : it.h0;
       const int row = qt * kTile + r;
       const bool in_rows = row < p.nq;
+      const int nsl = ist->tile[wg].nsl;
+      // this row's visible keys once per item; PARTIAL tiles clip them instead of rereading
+      // the slice list (rows whose union needs more than two intervals use the list)
+      int ilo0, ihi0, ilo1, ihi1;
+      bool ivl_ok;
+      if (nsl >= 0 && nsl <= kStageSl) {
+        ivl_ok = row_intervals_of(
+            row, nsl,
+            [&](int k, int4& s4, int& type) {
+              s4 = ist->tile[wg].s[k];
+              type = ist->tile[wg].type[k];
+            },
+            ilo0, ihi0, ilo1, ihi1);
+      } else {
+        const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
+        ivl_ok = row_intervals(p, row, nsl, sl, ilo0, ihi0, ilo1, ihi1);
+      }
+      const uint32_t e_first = ist->e_first[kKS ? wg : 0];
       // this warpgroup's key tiles: entries j0, j0 + step, ... of the chunk (key split: every
       // other one, starting at the warpgroup's index)
       constexpr int step = kKS ? 2 : 1;
@@ -404,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.plan.part_lse[prow] = -INFINITY;
           }
         }
+        mbar_arrive(&it_empty[ib]);
         continue;
       }
       const uint32_t* ents = it.ents;
@@ -415,13 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         a_pos = row / p.alibi_pack;
       }
       const float slope_log2 = kBias ? p.alibi[a_head] * kLog2e : 0.0f;
-      const int nsl = qt < p.nqt ? p.plan.row_nsl[qt] : 0;
-      const int* sl = p.plan.row_sl + static_cast<size_t>(qt < p.nqt ? qt : 0) * kSliceCap;
-      // this row's visible keys once per item; PARTIAL tiles clip them instead of rereading
-      // the slice list (rows whose union needs more than two intervals use the list)
-      int ilo0, ihi0, ilo1, ihi1;
-      const bool ivl_ok = row_intervals(p, row, nsl, sl, ilo0, ihi0, ilo1, ihi1);
-      uint32_t e_next = ents[j0];
+      uint32_t e_next = e_first;
       // l_run: sum of the fp32 p (for the LSE); r_run: sum of the bf16-rounded p that the PV
       // MMA actually multiplies (normalising O by it keeps the weights a convex combination,
       // so a dominant key is reproduced exactly even when the reference max is stale).  On
@@ -451,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // element mask of this row over the tile (bit c: key kt * 128 + c visible)
         uint32_t wm[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
         if (!kFixed && masked) {  // (the bounded-softcap kernel masks inside its own pass)
-          tile_mask(p, cls, row, kt, nsl, sl, ivl_ok, ilo0, ihi0, ilo1, ihi1, wm);
+          tile_mask(p, cls, row, kt, &ist->tile[wg].nsl, qt, ivl_ok, ilo0, ihi0, ilo1, ihi1, wm);
           // none of the warp's 32 rows sees a key of this tile (a decoding batch's tile
           // belongs to one sequence; rows past the end): P = 0, nothing else changes
           if (__all_sync(0xffffffffu, (wm[0] | wm[1] | wm[2] | wm[3]) == 0u)) {
@@ -494,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __float_as_uint(capped_log2(__uint_as_float(sv[c >> 5][c & 31]), p.cap_c, p.cap_k));
           }
           uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-          if (masked) tile_mask(p, cls, row, kt, nsl, sl, ivl_ok, ilo0, ihi0, ilo1, ihi1, w);
+          if (masked) tile_mask(p, cls, row, kt, &ist->tile[wg].nsl, qt, ivl_ok, ilo0, ihi0, ilo1, ihi1, w);
           float2 sum2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
           float2 sumr2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
           const float2 nm2 = make_float2(-p.cap_c, -p.cap_c);
@@ -724,44 +795,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = r_run > 0.0f ? 1.0f / r_run : 0.0f;
       const float lse_row = l_run > 0.0f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
-      if (it.pslot < 0) {
+      // the item's head and partial slot, decoded again from the staging slot here rather than
+      // held in registers through the tile loop
+      const Item ie = decode_item<kKS>(p, item, ist->ch);
+      const int he = wg ? ie.h1 : ie.h0;
+      if (ie.pslot < 0) {
         // O through shared memory: each 64-column box of the tile is written row by row into
         // the staging box (128-byte swizzle: 16-byte chunk k of row r at chunk k ^ (r % 8)) and
         // stored with one TMA copy, which leaves out the rows past the end
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) {
+          // the box's 64 columns are read and packed while the previous copy out of the
+          // staging box may still be reading it
+          uint32_t o[2][32];
+          tmem_ld32(tO + 64 * b, o[0]);
+          tmem_ld32(tO + 64 * b + 32, o[1]);
+          tmem_wait_ld();
+          reg_fence(o[0]);
+          reg_fence(o[1]);
+          uint4 v[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t* ok8 = o[k >> 2] + 8 * (k & 3);
+            v[k].x = pack_bf16x2(__uint_as_float(ok8[0]) * inv_l, __uint_as_float(ok8[1]) * inv_l);
+            v[k].y = pack_bf16x2(__uint_as_float(ok8[2]) * inv_l, __uint_as_float(ok8[3]) * inv_l);
+            v[k].z = pack_bf16x2(__uint_as_float(ok8[4]) * inv_l, __uint_as_float(ok8[5]) * inv_l);
+            v[k].w = pack_bf16x2(__uint_as_float(ok8[6]) * inv_l, __uint_as_float(ok8[7]) * inv_l);
+          }
           // the previous copy out of the staging box has read it
           if (leader) bulk_wait_group_read<0>();
           named_bar_sync(1 + wg, 128);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + 64 * b + 32 * c, o);
-            tmem_wait_ld();
-            reg_fence(o);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-              v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-              v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-              v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-              const int chunk = (4 * c + k) ^ (r & 7);
-              *reinterpret_cast<uint4*>(ost + r * 128 + chunk * 16) = v;
-            }
-          }
+          for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ost + r * 128 + ((k ^ (r & 7)) * 16)) = v[k];
           fence_proxy_async_smem();
           named_bar_sync(1 + wg, 128);
           if (leader) {
-            tma_store_2d(&tmO, ost, h * D + 64 * b, qt * kTile);
+            tma_store_2d(&tmO, ost, he * D + 64 * b, qt * kTile);
             bulk_commit_group();
           }
         }
-        if (in_rows) p.lse[static_cast<size_t>(h) * p.nq + row] = lse_row;
+        if (in_rows) p.lse[static_cast<size_t>(he) * p.nq + row] = lse_row;
       } else {
         // one chunk of a split row: normalised partial O (fp32) and its LSE for the merge
         // (rows past the end are never merged)
-        const size_t prow = (static_cast<size_t>(it.pslot) * p.slots + it.slot) * 2 * kTile + wg * kTile + r;
+        const size_t prow = (static_cast<size_t>(ie.pslot) * p.slots + ie.slot) * 2 * kTile + wg * kTile + r;
         float4* dst = reinterpret_cast<float4*>(p.plan.part_o + prow * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -779,6 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (in_rows) p.plan.part_lse[prow] = lse_row;
       }
+      mbar_arrive(&it_empty[ib]);  // the item's staging slot is no longer read
     }
     if (!ok) record_abort(abort_flag, p.status);
     if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // output copies done
@@ -988,6 +1066,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(drain);
       mbar_wait(drain, 0, nullptr, 100000000ull);
     }
+    __syncwarp();
+  } else if (warp == kWarpDec) {
+    // ------------------------------------------------------------ item decoder
+    // Stages each item while the softmax warpgroups still work on the one before it, so that
+    // the chain of dependent loads behind an item (chunk order, chunk, the query tile's slice
+    // list, its slices, the first entry) is off their path at the item boundary.  Lanes 0-7: query tile t = lane / 4,
+    // staged slice k = lane % 4; lanes 8-9: first entries; lane 10: the item's chunk.
+    bool ok = true;
+    for (int wave = 0; ok; ++wave) {
+      const int item = sched_item(wave);
+      if (item >= n_items) break;
+      const int ib = wave & 1;
+      if (wave >= 2) {  // the softmax threads have read this slot's previous item
+        ok = __all_sync(0xffffffffu, mbar_wait(&it_empty[ib], ((wave >> 1) - 1) & 1u, abort_flag, lim));
+        if (!ok) break;
+      }
+      ItemStage* ist = reinterpret_cast<ItemStage*>(sm + SM::kIt) + ib;
+      const int4 ch = item_chunk(p, item);
+      const Item it = decode_item<kKS>(p, item, ch);
+      const int t = (lane >> 2) & 1, k = lane & 3;
+      const int qt = t ? it.qt1 : it.qt0;
+      if (lane < 8) {
+        int nsl = 0, si = 0;
+        if (qt < p.nqt) {
+          nsl = p.plan.row_nsl[qt];
+          si = p.plan.row_sl[static_cast<size_t>(qt) * kSliceCap + k];
+        }
+        if (k < nsl) {
+          ist->tile[t].s[k] = p.plan.slices[si];
+          ist->tile[t].type[k] = p.plan.stypes[si];
+        }
+        if (k == 0) ist->tile[t].nsl = nsl;
+      } else if (lane < 10) {
+        const int j = lane - 8;
+        ist->e_first[j] = j < it.n ? it.ents[j] : 0u;
+      } else if (lane == 10) {
+        ist->ch = ch;
+      }
+      mbar_arrive(&it_full[ib]);
+    }
+    if (!ok) record_abort(abort_flag, p.status);
     __syncwarp();
   }
   }  // producer warpgroup
