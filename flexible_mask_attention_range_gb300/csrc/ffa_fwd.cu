@@ -404,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
+  pdl_wait();  // the planner's kernels have completed (everything above overlapped their tail)
   const int n_items = p.plan.hdr[1] * p.slots;  // chunks x head slots, written by the planner
   // K/V ring: S slots, one more with the key split (see FwdSmem)
   constexpr uint32_t nst = kKS ? S + 1 : S;
@@ -1294,9 +1295,11 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
   if (grid <= 0) return cudaSuccess;
   if (g_kernel_events.fwd_start != nullptr) cudaEventRecord(g_kernel_events.fwd_start, stream);
-  kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, mo, p);
+  // a programmatic dependent of the planner's last kernel: the CTAs set up their barriers and
+  // TMEM while it finishes (with a timing event recorded in between, plain stream order)
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreads), SM::kAlloc, stream, mq, mk, mv, mo, p);
   if (g_kernel_events.fwd_stop != nullptr) cudaEventRecord(g_kernel_events.fwd_stop, stream);
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || !a.split) return e;
   ffa_fwd_merge<D><<<a.ngrp * a.slots * (a.key_split ? 1 : 2) * kTile, 32 * kMergeWarps, 0, stream>>>(p);
   return cudaGetLastError();

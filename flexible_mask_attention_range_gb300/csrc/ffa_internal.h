@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/ffa.h"
 
@@ -194,6 +195,33 @@ struct PlanView {
   uint32_t* col_ent;     // [nkt, nqt]
   int* col_order;
 };
+
+// Programmatic dependent launch.  A kernel launched by launch_pdl may begin while the kernel
+// before it in the stream is still running (once every block of that kernel has called
+// pdl_launch_dependents or exited), which hides the launch gap between the short planner
+// kernels and the attention kernel.  Such a kernel calls pdl_wait() before it touches global
+// memory that an earlier kernel of the stream writes or reads: the wait returns once the
+// kernel before it has completed and its writes are visible (and that kernel itself waited for
+// the one before it, or was launched in plain stream order).  Without the launch attribute
+// both calls do nothing.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 inline PlanView plan_view(const WsLayout& L, void* ws) {
   char* b = static_cast<char*>(ws);

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(1024) plan_slices_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ ty, int R, int nq, int nk,
                                                            PlanView v, int32_t* status) {
   __shared__ int warp_buf[32];
+  pdl_launch_dependents();  // (launched in stream order: the next planner kernel may start)
   int base = 0, bad = 0;
   for (int c = 0; c < R; c += blockDim.x) {
     const int r = c + threadIdx.x;
@@ -192,6 +193,8 @@ __global__ void __launch_bounds__(256) plan_row_classes_kernel(ProblemDims P, Pl
   __shared__ int4 sm_s[kSliceSmem];
   __shared__ int sm_t[kSliceSmem];
   __shared__ int warp_buf[32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int qt = blockIdx.x;
   const int k0 = blockIdx.y * kPlanSpan, k1 = min(P.nkt, k0 + kPlanSpan);
   const int n_valid = v.hdr[0];
@@ -214,6 +217,8 @@ __global__ void __launch_bounds__(256) plan_row_classes_kernel(ProblemDims P, Pl
 constexpr int kListRun = 16;
 __global__ void __launch_bounds__(256) plan_row_lists_kernel(ProblemDims P, int head_pair, PlanView v) {
   __shared__ int warp_buf[32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int g = blockIdx.x;
   const int qa = head_pair ? g : 2 * g, qb = head_pair ? g : 2 * g + 1;
   const uint8_t* ca_row = v.cls + static_cast<size_t>(qa) * P.nkt;
@@ -248,6 +253,8 @@ __global__ void __launch_bounds__(256) plan_cols_kernel(ProblemDims P, PlanView 
   __shared__ int4 sm_s[kSliceSmem];
   __shared__ int sm_t[kSliceSmem];
   __shared__ int warp_buf[32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int kt = blockIdx.x;
   const int n_valid = v.hdr[0];
   const int c0 = kt * kTile, c1 = min(c0 + kTile, P.nk);
@@ -328,6 +335,8 @@ __global__ void __launch_bounds__(1024) plan_order_kernel(const int* __restrict_
                                                           int* __restrict__ order) {
   extern __shared__ int hist[];
   __shared__ int warp_buf[32];
+  pdl_wait();
+  pdl_launch_dependents();
   counting_sort_desc(cnt, n, max_len, order, hist, warp_buf);
 }
 
@@ -339,6 +348,8 @@ __global__ void __launch_bounds__(1024) plan_order_kernel(const int* __restrict_
 __global__ void __launch_bounds__(1024) plan_chunks_kernel(int ngrp, int split_len, int all_split, PlanView v) {
   extern __shared__ int hist[];  // split_len + 1
   __shared__ int warp_buf[32];
+  pdl_wait();
+  pdl_launch_dependents();
   int base = 0, pbase = 0;
   for (int c = 0; c < ngrp; c += blockDim.x) {
     const int g = c + threadIdx.x;
@@ -405,26 +416,24 @@ cudaError_t launch_plan_slices(const ProblemDims& P, const int32_t* q_ranges, co
 
 cudaError_t launch_plan_rows(const ProblemDims& P, const WsLayout& L, const PlanView& v, cudaStream_t s) {
   if (L.ngrp == 0) return cudaSuccess;
-  plan_row_classes_kernel<<<dim3(P.nqt, (P.nkt + kPlanSpan - 1) / kPlanSpan), 256, 0, s>>>(P, v);
-  cudaError_t e = cudaGetLastError();
+  // (each launched as a programmatic dependent of the planner kernel before it)
+  cudaError_t e = launch_pdl(plan_row_classes_kernel, dim3(P.nqt, (P.nkt + kPlanSpan - 1) / kPlanSpan), dim3(256),
+                             0, s, P, v);
   if (e != cudaSuccess) return e;
   // a key-split group is one query tile, as a head pair's is
-  plan_row_lists_kernel<<<L.ngrp, 256, 0, s>>>(P, (L.head_pair || L.key_split) ? 1 : 0, v);
-  e = cudaGetLastError();
+  e = launch_pdl(plan_row_lists_kernel, dim3(L.ngrp), dim3(256), 0, s, P, (L.head_pair || L.key_split) ? 1 : 0, v);
   if (e != cudaSuccess) return e;
   const size_t smem = static_cast<size_t>(L.split_len + 1) * sizeof(int);
-  plan_chunks_kernel<<<1, 1024, smem, s>>>(L.ngrp, L.split_len, L.key_split ? 1 : 0, v);
-  return cudaGetLastError();
+  return launch_pdl(plan_chunks_kernel, dim3(1), dim3(1024), smem, s, L.ngrp, L.split_len, L.key_split ? 1 : 0, v);
 }
 
 cudaError_t launch_plan_cols(const ProblemDims& P, const PlanView& v, cudaStream_t s) {
   if (P.nkt == 0) return cudaSuccess;
-  plan_cols_kernel<<<P.nkt, 256, 0, s>>>(P, v);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(plan_cols_kernel, dim3(P.nkt), dim3(256), 0, s, P, v);
   if (e != cudaSuccess) return e;
   const size_t smem = static_cast<size_t>(P.nqt + 1) * sizeof(int);
-  plan_order_kernel<<<1, 1024, smem, s>>>(v.col_cnt, P.nkt, P.nqt, v.col_order);
-  return cudaGetLastError();
+  return launch_pdl(plan_order_kernel, dim3(1), dim3(1024), smem, s, static_cast<const int*>(v.col_cnt), P.nkt, P.nqt,
+                    v.col_order);
 }
 
 }  // namespace ffa
