@@ -544,10 +544,10 @@ def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
 # source changes the figure no longer describes the kernel, and `traffic` is reported null.
 TRAFFIC = {
     # (workload, kernel): (bytes per launch, source hash at capture)
-    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1862966016 + 239055104, "1f9fd45814c0fd8c"),
-    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (23660692992 + 12239583744, "c5d2c680902023ff"),
-    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541005056 + 241070592, "1f9fd45814c0fd8c"),
-    ("sliding_32k_softcap", "ffa_bwd_kernel"): (2688512256 + 1354383872, "c5d2c680902023ff"),
+    ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1856736000 + 238412032, "388d8b2834b203d0"),
+    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (24077428992 + 12629843456, "f1d154e1b498bb66"),
+    ("sliding_32k_softcap", "ffa_fwd_kernel"): (541080320 + 240462336, "388d8b2834b203d0"),
+    ("sliding_32k_softcap", "ffa_bwd_kernel"): (2688905984 + 1354405376, "f1d154e1b498bb66"),
 }
 
 

@@ -183,7 +183,8 @@ int fwd_launch(const FwdCall& c, const WsLayout& L, void* scratch) {
   }
   const ProblemDims P = dims_of(L);
   const PlanView pv = plan_view(L, scratch);
-  cudaError_t e = launch_plan_slices(P, c.q_ranges, c.k_ranges, c.types, c.n_ranges, pv, c.status, s);
+  cudaError_t e =
+      launch_plan_slices(P, c.q_ranges, c.k_ranges, c.types, c.n_ranges, pv, c.status, s, c.after_own_kernel);
   if (e == cudaSuccess) e = launch_plan_rows(P, L, pv, s);
   if (e != cudaSuccess) return FFA_ERR_CUDA;
   FwdArgs a;

@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
+  pdl_wait();  // the preprocess has completed (the setup above overlapped its tail)
 
   if (warp < 8) {
     // ------------------------------------------------------------ compute warpgroups
@@ -815,6 +816,8 @@ __global__ void __launch_bounds__(256) ffa_bwd_pre(const __nv_bfloat16* __restri
                                                    const float* __restrict__ lse, float* __restrict__ rowD,
                                                    float* __restrict__ lse2, float* __restrict__ dqacc, int nq,
                                                    int hq, int qpad) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const size_t nwarps = static_cast<size_t>(gridDim.x) * (blockDim.x >> 5);
   const size_t total = static_cast<size_t>(qpad) * hq;
@@ -847,6 +850,7 @@ __global__ void __launch_bounds__(256) ffa_bwd_pre(const __nv_bfloat16* __restri
 
 __global__ void __launch_bounds__(256) ffa_bwd_dq_convert(const float* __restrict__ acc,
                                                           __nv_bfloat16* __restrict__ dq, size_t n) {
+  pdl_wait();
   const size_t n4 = n / 4;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -877,10 +881,12 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   {
     const size_t warps = static_cast<size_t>(qpad) * P.hq;
     const int blocks = static_cast<int>(std::min<size_t>((warps + 7) / 8, static_cast<size_t>(nsm) * 16));
-    ffa_bwd_pre<D><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(a.out),
-                                                static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.rowD, a.lse2,
-                                                a.dqacc, P.nq, P.hq, qpad);
-    cudaError_t e = cudaGetLastError();
+    // programmatic dependents from here on: each kernel's launch overlaps the tail of the one
+    // before it and waits (pdl_wait) before it touches what that one writes
+    cudaError_t e = launch_pdl(ffa_bwd_pre<D>, dim3(blocks), dim3(256), 0, stream,
+                               static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout),
+                               static_cast<const float*>(a.lse), a.rowD, a.lse2, a.dqacc, static_cast<int>(P.nq), P.hq,
+                               qpad);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mq, mk, mv, mdo, mdq;
@@ -930,7 +936,8 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
                                                    args, SM::kAlloc, stream);
       if (le != cudaSuccess) return le;
     } else {
-      kern<<<grid, kThreads, SM::kAlloc, stream>>>(mq, mk, mv, mdo, mdq, p);
+      cudaError_t le = launch_pdl(kern, dim3(grid), dim3(kThreads), SM::kAlloc, stream, mq, mk, mv, mdo, mdq, p);
+      if (le != cudaSuccess) return le;
     }
     if (g_kernel_events.bwd_stop != nullptr) cudaEventRecord(g_kernel_events.bwd_stop, stream);
     cudaError_t e = cudaGetLastError();
@@ -938,8 +945,13 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   }
   const size_t n = static_cast<size_t>(P.nq) * P.hq * D;
   const int blocks = static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, static_cast<size_t>(nsm) * 8));
-  if (blocks > 0) ffa_bwd_dq_convert<<<blocks, 256, 0, stream>>>(a.dqacc, static_cast<__nv_bfloat16*>(a.dq), n);
-  return cudaGetLastError();
+  if (blocks <= 0) return cudaSuccess;
+  if (kDet) {  // (after the cooperative launch: plain stream order)
+    ffa_bwd_dq_convert<<<blocks, 256, 0, stream>>>(a.dqacc, static_cast<__nv_bfloat16*>(a.dq), n);
+    return cudaGetLastError();
+  }
+  return launch_pdl(ffa_bwd_dq_convert, dim3(blocks), dim3(256), 0, stream, static_cast<const float*>(a.dqacc),
+                    static_cast<__nv_bfloat16*>(a.dq), n);
 }
 
 }  // namespace

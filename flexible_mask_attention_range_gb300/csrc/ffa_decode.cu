@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(256) decode_prepare(const uint4* __restrict__ 
                                                       const int32_t* __restrict__ ty, int R, int M, int64_t nk,
                                                       int32_t* __restrict__ qr2, int32_t* __restrict__ kr2,
                                                       int32_t* __restrict__ ty2, int32_t* status) {
+  pdl_launch_dependents();  // the planner's first kernel may start (it waits for this one)
   if (static_cast<int>(blockIdx.x) < pack_blocks)
     decode_pack_q(q, qp, n, hq, P, d, blockIdx.x, pack_blocks);
   else
@@ -208,6 +209,7 @@ int ffa_fwd_decode(const ffa_shape* shape, const void* q, const void* k, const v
   c.status = status; c.stream = stream; c.options = options;
   c.alibi_pack = P;
   c.key_split = true;
+  c.after_own_kernel = true;
   // every packed row goes through the LSE merge, which writes the caller's layout directly
   c.unpack_out = out;
   c.unpack_lse = lse;

@@ -1134,6 +1134,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) ffa_fwd_merge(const FwdParam
   __shared__ float sh_acc[kMergeWarps][D];
   __shared__ float sh_w[kMergeWarps];
   __shared__ float sh_max[kMergeWarps];
+  pdl_wait();  // the attention kernel's partial results are complete
   int b = blockIdx.x;
   const int r = b % kTile;
   b /= kTile;
@@ -1301,8 +1302,8 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t stream) {
   if (g_kernel_events.fwd_stop != nullptr) cudaEventRecord(g_kernel_events.fwd_stop, stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || !a.split) return e;
-  ffa_fwd_merge<D><<<a.ngrp * a.slots * (a.key_split ? 1 : 2) * kTile, 32 * kMergeWarps, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(ffa_fwd_merge<D>, dim3(a.ngrp * a.slots * (a.key_split ? 1 : 2) * kTile), dim3(32 * kMergeWarps),
+                    0, stream, p);
 }
 
 template <bool kKS>

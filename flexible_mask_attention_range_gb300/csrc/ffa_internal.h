@@ -254,8 +254,11 @@ struct ProblemDims {
 };
 
 // Planner launches (ffa_plan.cu).  Each returns a cudaError_t of the launches.
+// (dependent: launched as a programmatic dependent of the kernel before it, which must be
+// one of this library's)
 cudaError_t launch_plan_slices(const ProblemDims& P, const int32_t* q_ranges, const int32_t* k_ranges,
-                               const int32_t* types, int R, const PlanView& v, int32_t* status, cudaStream_t s);
+                               const int32_t* types, int R, const PlanView& v, int32_t* status, cudaStream_t s,
+                               bool dependent = false);
 cudaError_t launch_plan_rows(const ProblemDims& P, const WsLayout& L, const PlanView& v, cudaStream_t s);
 cudaError_t launch_plan_cols(const ProblemDims& P, const PlanView& v, cudaStream_t s);
 cudaError_t launch_plan_ranks(const ProblemDims& P, const PlanView& v, int* tile_rank, cudaStream_t s);
@@ -333,6 +336,9 @@ struct FwdCall {
   bool key_split = false;  // WsLayout::key_split (decode)
   void* unpack_out = nullptr;  // FwdArgs::unpack_out
   float* unpack_lse = nullptr;
+  // the stream's last operation is a kernel of this library (decode: the packing kernel), so
+  // the planner's first kernel may be launched as its programmatic dependent
+  bool after_own_kernel = false;
 };
 // Shape check shared by the entry points (FFA_OK or the error code).
 int check_shape(const ffa_shape* s, int32_t n_ranges);

@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(1024) plan_slices_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ ty, int R, int nq, int nk,
                                                            PlanView v, int32_t* status) {
   __shared__ int warp_buf[32];
-  pdl_launch_dependents();  // (launched in stream order: the next planner kernel may start)
+  pdl_wait();  // (launched as a dependent of the decode packing kernel, which writes the slices)
+  pdl_launch_dependents();
   int base = 0, bad = 0;
   for (int c = 0; c < R; c += blockDim.x) {
     const int r = c + threadIdx.x;
@@ -409,7 +410,11 @@ cudaError_t launch_plan_ranks(const ProblemDims& P, const PlanView& v, int* tile
 }
 
 cudaError_t launch_plan_slices(const ProblemDims& P, const int32_t* q_ranges, const int32_t* k_ranges,
-                               const int32_t* types, int R, const PlanView& v, int32_t* status, cudaStream_t s) {
+                               const int32_t* types, int R, const PlanView& v, int32_t* status, cudaStream_t s,
+                               bool dependent) {
+  if (dependent)
+    return launch_pdl(plan_slices_kernel, dim3(1), dim3(1024), 0, s, q_ranges, k_ranges, types, R,
+                      static_cast<int>(P.nq), static_cast<int>(P.nk), v, status);
   plan_slices_kernel<<<1, 1024, 0, s>>>(q_ranges, k_ranges, types, R, P.nq, P.nk, v, status);
   return cudaGetLastError();
 }
