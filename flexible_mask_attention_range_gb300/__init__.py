@@ -171,6 +171,12 @@ def ffa_bwd_workspace_size(total_q, total_k, num_heads_q, num_heads_kv, head_dim
     return int(lib().ffa_bwd_workspace_size(ctypes.byref(s), int(n_ranges)))
 
 
+def ffa_fwd_decode_workspace_size(total_q, total_k, num_heads_q, num_heads_kv, head_dim, n_ranges,
+                                  max_seqlen_q) -> int:
+    s = _shape(total_q, total_k, num_heads_q, num_heads_kv, head_dim)
+    return int(lib().ffa_fwd_decode_workspace_size(ctypes.byref(s), int(n_ranges), int(max_seqlen_q)))
+
+
 def ffa_status_string(code: int) -> str:
     return lib().ffa_status_string(int(code)).decode()
 
