@@ -545,9 +545,9 @@ def per_config(ffa, dev, peaks, iters: int = 10, warm: int = 3):
 TRAFFIC = {
     # (workload, kernel): (bytes per launch, source hash at capture)
     ("long_causal_64k_prefix", "ffa_fwd_kernel"): (1856736000 + 238412032, "388d8b2834b203d0"),
-    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (24077428992 + 12629843456, "f1d154e1b498bb66"),
+    ("long_causal_64k_prefix", "ffa_bwd_kernel"): (23225705728 + 11979547904, "743ef98528ce98e7"),
     ("sliding_32k_softcap", "ffa_fwd_kernel"): (541080320 + 240462336, "388d8b2834b203d0"),
-    ("sliding_32k_softcap", "ffa_bwd_kernel"): (2688905984 + 1354405376, "f1d154e1b498bb66"),
+    ("sliding_32k_softcap", "ffa_bwd_kernel"): (2695739392 + 1358949376, "743ef98528ce98e7"),
 }
 
 

@@ -809,7 +809,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // -D_i = -(dO_i . O_i) and -LSE_i * log2(e) per (head, row), padded to whole tiles (stored
 // negated so the main kernel adds them with packed pair instructions); zero the dq
-// accumulator.  One warp per (row, head).
+// accumulator.  D / 8 lanes per (row, head), 16 bytes of O and of dO per lane, and kUnroll
+// row groups per warp pass with every load issued before the first use, so that enough
+// bytes are in flight to run at the copy bandwidth.
 template <int D>
 __global__ void __launch_bounds__(256) ffa_bwd_pre(const __nv_bfloat16* __restrict__ out,
                                                    const __nv_bfloat16* __restrict__ dout,
@@ -818,32 +820,56 @@ __global__ void __launch_bounds__(256) ffa_bwd_pre(const __nv_bfloat16* __restri
                                                    int hq, int qpad) {
   pdl_wait();
   pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
+  constexpr int kLanes = D / 8;          // lanes of one (row, head)
+  constexpr int kRows = 32 / kLanes;     // (row, head) units per warp and group
+  constexpr int kUnroll = 4;
+  constexpr int kPass = kRows * kUnroll;  // units per warp pass
+  const int lane = threadIdx.x & 31, sub = lane / kLanes, sl = lane % kLanes;
   const size_t nwarps = static_cast<size_t>(gridDim.x) * (blockDim.x >> 5);
   const size_t total = static_cast<size_t>(qpad) * hq;
-  for (size_t wi = blockIdx.x * static_cast<size_t>(blockDim.x >> 5) + (threadIdx.x >> 5); wi < total;
-       wi += nwarps) {
-    const int h = static_cast<int>(wi / qpad);
-    const int i = static_cast<int>(wi - static_cast<size_t>(h) * qpad);
-    float dsum = 0.0f, l2 = -INFINITY;
-    if (i < nq) {
-      const size_t base = (static_cast<size_t>(i) * hq + h) * D;
-      constexpr int kPer = D / 32;  // 2 or 4 elements per lane
-      const __nv_bfloat16* a = out + base + lane * kPer;
-      const __nv_bfloat16* b = dout + base + lane * kPer;
+  for (size_t w0 = (blockIdx.x * static_cast<size_t>(blockDim.x >> 5) + (threadIdx.x >> 5)) * kPass; w0 < total;
+       w0 += nwarps * kPass) {
+    uint4 a[kUnroll], b[kUnroll];
+    size_t base[kUnroll];
+    bool live[kUnroll];
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) dsum += __bfloat162float(a[e]) * __bfloat162float(b[e]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-      float* z = dqacc + base + lane * kPer;
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) z[e] = 0.0f;
-      const float l = lse[static_cast<size_t>(h) * nq + i];
-      l2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t wi = w0 + u * kRows + sub;
+      const int h = static_cast<int>(wi / qpad);
+      const int i = static_cast<int>(wi - static_cast<size_t>(h) * qpad);
+      live[u] = wi < total && i < nq;
+      base[u] = live[u] ? (static_cast<size_t>(i) * hq + h) * D + sl * 8 : 0;
+      a[u] = live[u] ? *reinterpret_cast<const uint4*>(out + base[u]) : make_uint4(0u, 0u, 0u, 0u);
+      b[u] = live[u] ? *reinterpret_cast<const uint4*>(dout + base[u]) : make_uint4(0u, 0u, 0u, 0u);
     }
-    if (lane == 0) {
-      rowD[wi] = i < nq ? -dsum : 0.0f;
-      lse2[wi] = l2;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, bv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+      float dsum = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dsum += __uint_as_float(av[e] << 16) * __uint_as_float(bv[e] << 16);
+        dsum += __uint_as_float(av[e] & 0xffff0000u) * __uint_as_float(bv[e] & 0xffff0000u);
+      }
+#pragma unroll
+      for (int o = kLanes / 2; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+      const size_t wi = w0 + u * kRows + sub;
+      if (live[u]) {
+        float4* z = reinterpret_cast<float4*>(dqacc + base[u]);
+        z[0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        z[1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+      if (sl == 0 && wi < total) {
+        const int h = static_cast<int>(wi / qpad);
+        const int i = static_cast<int>(wi - static_cast<size_t>(h) * qpad);
+        float l2 = -INFINITY;
+        if (i < nq) {
+          const float l = lse[static_cast<size_t>(h) * nq + i];
+          l2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+        }
+        rowD[wi] = i < nq ? -dsum : 0.0f;
+        lse2[wi] = l2;
+      }
     }
   }
 }
@@ -879,7 +905,8 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t stream) {
   const int qpad = P.nqt * kTile;
   const int nsm = num_sms();
   {
-    const size_t warps = static_cast<size_t>(qpad) * P.hq;
+    // (row, head) units over warps of D / 8 lanes per unit, four groups per warp pass
+    const size_t warps = (static_cast<size_t>(qpad) * P.hq * (D / 8) / 32 + 3) / 4;
     const int blocks = static_cast<int>(std::min<size_t>((warps + 7) / 8, static_cast<size_t>(nsm) * 16));
     // programmatic dependents from here on: each kernel's launch overlaps the tail of the one
     // before it and waits (pdl_wait) before it touches what that one writes
