@@ -50,6 +50,22 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
+def headline_peak(peaks: dict, clocks: dict):
+    """(peak TFLOP/s, name) for the headline fractions: the burst cuBLAS bf16 figure unless the
+    median SM clock of the timed region was nearer the clock the sustained figure was measured
+    at (its median under load) than the maximum, then the sustained figure; without that
+    record, the burst figure unless the clock was below 97 % of the maximum.  No clock record:
+    the sustained figure."""
+    peak_burst = float(peaks.get("bf16_tflops", 1900.0))
+    peak_sust = float(peaks.get("bf16_tflops_sustained", peak_burst))
+    sust_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+    at_max = False
+    if clocks.get("sm_mhz") is not None and clocks.get("sm_max_mhz"):
+        thr = 0.5 * (float(sust_mhz) + clocks["sm_max_mhz"]) if sust_mhz else 0.97 * clocks["sm_max_mhz"]
+        at_max = clocks["sm_mhz"] >= thr
+    return (peak_burst, "bf16_tflops (burst)") if at_max else (peak_sust, "bf16_tflops_sustained")
+
+
 def visible_pairs(w: W.Workload) -> int:
     """Exact visible-pair count from the slice list (per-row interval union, host-side)."""
     # Rows are processed in blocks; each row's visible set is the union of one interval per
@@ -324,17 +340,9 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local: int):
 
     bwd_tf = fl_bwd / (bwd_ms * 1e-3) / 1e12
     fwd_tf = fl_fwd / (fwd_ms * 1e-3) / 1e12
-    # headline peak: the burst cuBLAS figure unless the SM clock during the timed region was
-    # nearer the clock the sustained figure was measured at (its median under load) than the
-    # maximum; without that record, the burst figure unless the clock was below 97 % of max
     peak_burst = float(peaks.get("bf16_tflops", 1900.0))
     peak_sust = float(peaks.get("bf16_tflops_sustained", peak_burst))
-    sust_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
-    at_max = False
-    if clocks.get("sm_mhz") is not None and clocks.get("sm_max_mhz"):
-        thr = 0.5 * (float(sust_mhz) + clocks["sm_max_mhz"]) if sust_mhz else 0.97 * clocks["sm_max_mhz"]
-        at_max = clocks["sm_mhz"] >= thr
-    peak_t, peak_kind = (peak_burst, "bf16_tflops (burst)") if at_max else (peak_sust, "bf16_tflops_sustained")
+    peak_t, peak_kind = headline_peak(peaks, clocks)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
